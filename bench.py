@@ -1,0 +1,387 @@
+#!/usr/bin/env python
+"""Benchmark of the dropless MoE expert layer on GB300: one step = route +
+forward + backward of one layer over one batch of synthetic tokens.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 235b]
+  python bench.py --impl reference ...      # the float64 CPU oracle arm
+
+Metric: per-layer training-step throughput in algorithmic TFLOP/s
+(18 * T * top_k * H * I per step: 6 forward + 12 backward), plus per-pass
+forward / backward ms.  Prints ONE JSON line on rank 0.
+
+Default workload: the Qwen3-235B-A22B layer shape (T=16384, H=4096, E=128,
+top_k=8, I=1536, bf16), the shape at which the tensor-roofline target is
+stated.  Inputs are seeded synthetic draws (``workloads``); the per-step
+working set (4.8 GB of weights, 0.1 GB of tokens) is far larger than the
+129 MB L2, so no L2 flush is needed between steps.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from workloads import CONFIGS, make_inputs  # noqa: E402
+
+LAUNCHES_PER_STEP = 11   # route 3, forward 4, backward 4 (bf16 path)
+CPU_SAMPLE_EXPERTS = 16   # cpu_baseline: all assignments of 16 experts
+REF_SAMPLE_EXPERTS = 1    # reference arm: one expert per step (rotating)
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--workload", default="235b", choices=[k for k in CONFIGS if k != "tiny"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def _host_cores():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        n = [i["num_threads"] for i in info if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def _workload_desc(cfg):
+    return (f"{cfg.name}: MoE expert layer T={cfg.T} H={cfg.H} E={cfg.E} top_k={cfg.k} "
+            f"I={cfg.I}" + (" (Zipf-skewed routing, 8 empty experts)" if cfg.skew else ""))
+
+
+def _oracle_sample(cfg, inp, experts):
+    """The float64 oracle on a bounded sample of the workload: routing of the
+    whole batch, then forward + backward of every assignment of the given
+    experts (each expert's assignments form a k=1 sub-batch with their own
+    gates and the expert's weights).  Returns (seconds, algorithmic flops)."""
+    from oracle import moe_oracle as O
+    from workloads import bf16_bits_to_f32
+
+    def f32(a):
+        return bf16_bits_to_f32(a) if a.dtype == np.uint16 else a
+
+    t0 = time.perf_counter()
+    idx, gate = O.route(inp["logits"], cfg.k)
+    n_total = 0
+    for e in experts:
+        t, j = np.nonzero(idx == e)
+        if t.size == 0:
+            continue
+        n_total += t.size
+        sub_idx = np.zeros((t.size, 1), np.int32)
+        sub_gate = gate[t, j][:, None]
+        X = f32(inp["X"][t])
+        dY = f32(inp["dY"][t])
+        W13 = f32(inp["W13"][e:e + 1])
+        W2 = f32(inp["W2"][e:e + 1])
+        O.forward(X, W13, W2, sub_idx, sub_gate)
+        O.backward(X, W13, W2, sub_idx, sub_gate, dY)
+    dt = time.perf_counter() - t0
+    return dt, 18.0 * n_total * cfg.H * cfg.I
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _traffic(kernel, src_files):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    for f in src_files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    digest = h.hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            m = re.match(r"\|\s*(\S+)\s*\|\s*(\S+)\s*\|\s*([0-9.eE+]+)\s*\|", line)
+            if m and m.group(1) == kernel and m.group(2) == digest:
+                return float(m.group(3))
+    return None
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg = CONFIGS[args.workload]
+    inp = make_inputs(cfg)
+    times, flops = [], []
+    for i in range(args.warmup + args.steps):
+        experts = [(i * REF_SAMPLE_EXPERTS + q) % cfg.E for q in range(REF_SAMPLE_EXPERTS)]
+        dt, fl = _oracle_sample(cfg, inp, experts)
+        if i >= args.warmup:
+            times.append(dt)
+            flops.append(fl)
+    ms = 1e3 * statistics.mean(times)
+    value = sum(flops) / sum(times) / 1e12
+    cores = _host_cores()
+    sample = (f"float64 oracle: routing of the whole batch, then forward+backward of all "
+              f"assignments of {REF_SAMPLE_EXPERTS} expert(s) per step (rotating experts)")
+    print(json.dumps({
+        "impl": "reference", "metric": "moe_layer_step_tflops", "value": value,
+        "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": _workload_desc(cfg), "sample_experts": REF_SAMPLE_EXPERTS},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import mixture_experts_layer_18_gb300 as M
+    from mixture_experts_layer_18_gb300.layer import MoELayer
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group(backend="nccl")
+    torch.cuda.set_device(local)
+    cfg = CONFIGS[args.workload]
+    inp = make_inputs(cfg, seed=rank)
+
+    def dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+        return torch.from_numpy(a).cuda()
+
+    d = {k: dev(v) for k, v in inp.items()}
+    L = MoELayer(cfg.T, cfg.H, cfg.E, cfg.I, cfg.k, mode="bf16")
+    io = L.empty_io()
+
+    def fwd():
+        L.route(d["logits"])
+        L.forward(d["X"], d["W13"], d["W2"], io["Y"])
+
+    def bwd():
+        L.backward(d["dY"], d["W13"], d["W2"], io["dX"], io["dW13"], io["dW2"], io["dgate"])
+
+    def step():
+        fwd()
+        bwd()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if L.device_status() != 0:
+        raise RuntimeError(f"device status {L.device_status()} after warm-up")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def ev():
+        e = torch.cuda.Event(enable_timing=True)
+        return e
+
+    # ---- timed steps (kernel-level events around the backward GEMM launch)
+    K = args.steps
+    pairs_b = [(ev(), ev()) for _ in range(K)]
+    pairs_f = [(ev(), ev()) for _ in range(K)]
+    for a, b in pairs_b + pairs_f:       # materialise the event handles
+        a.record()
+        b.record()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.4)
+    barrier()
+    torch.cuda.synchronize()
+    t0, t1 = ev(), ev()
+    t0.record()
+    for i in range(K):
+        M.moe_set_gemm_events(M.MOE_WS_FORWARD, pairs_f[i][0].cuda_event, pairs_f[i][1].cuda_event)
+        fwd()
+        M.moe_set_gemm_events(M.MOE_WS_BACKWARD, pairs_b[i][0].cuda_event, pairs_b[i][1].cuda_event)
+        bwd()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms_step = t0.elapsed_time(t1) / K
+    gemm_b = statistics.mean(a.elapsed_time(b) for a, b in pairs_b)
+    gemm_f = statistics.mean(a.elapsed_time(b) for a, b in pairs_f)
+    if L.device_status() != 0:
+        raise RuntimeError(f"device status {L.device_status()} after timed steps")
+
+    # ---- per-pass timings
+    def timed(fn, n):
+        a, b = ev(), ev()
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    fwd_ms = timed(fwd, K)
+    bwd_ms = timed(bwd, K)
+
+    # ---- end to end: pinned host inputs in, results out, every step
+    h_in = {k: d[k].cpu().pin_memory() for k in ("logits", "X", "dY")}
+    h_out = {k: torch.empty(io[k].shape, dtype=io[k].dtype, pin_memory=True)
+             for k in ("Y", "dX", "dgate")}
+
+    def e2e_step():
+        for k, h in h_in.items():
+            d[k].copy_(h, non_blocking=True)
+        step()
+        for k, h in h_out.items():
+            h.copy_(io[k], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = timed(e2e_step, K)
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+
+    # ---- max over ranks
+    t = torch.tensor([ms_step, e2e_ms, fwd_ms, bwd_ms, gemm_b, gemm_f], device="cuda",
+                     dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_step, e2e_ms, fwd_ms, bwd_ms, gemm_b, gemm_f = t.tolist()
+
+    flops_step = cfg.fwd_flops() + cfg.bwd_flops()
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    peaks, src = _peaks()
+    peak = float(peaks["bf16_tflops"])
+    ach_b = cfg.bwd_flops() / (gemm_b * 1e-3) / 1e12
+    ach_f = cfg.fwd_flops() / (gemm_f * 1e-3) / 1e12
+    traffic = _traffic("moe_gemm_kernel<bf16,256>/backward",
+                       ["mixture_experts_layer_18_gb300/csrc/gemm.cu",
+                        "mixture_experts_layer_18_gb300/csrc/common.cuh"])
+    out = {
+        "metric": "moe_layer_step_tflops", "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": _workload_desc(cfg), "T": cfg.T, "H": cfg.H, "E": cfg.E,
+                   "top_k": cfg.k, "I": cfg.I, "mode": "bf16",
+                   "flops_per_step": flops_step, "parallelism": "replicas",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+        "fwd_tflops": cfg.fwd_flops() / (fwd_ms * 1e-3) / 1e12,
+        "bwd_tflops": cfg.bwd_flops() / (bwd_ms * 1e-3) / 1e12,
+        "roofline": {"kernel": "moe_gemm_kernel<bf16,256> (co-scheduled backward GEMMs)",
+                     "bound": "tensor", "achieved": ach_b, "peak": peak, "unit": "TFLOP/s",
+                     "frac": ach_b / peak, "traffic": traffic,
+                     "peak_source": f"{src} bf16_tflops (burst)", "launch_ms": gemm_b},
+        "roofline_forward_gemms": {"achieved": ach_f, "peak": peak, "frac": ach_f / peak,
+                                   "unit": "TFLOP/s", "launch_ms": gemm_f},
+        "e2e": {"value": world * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": LAUNCHES_PER_STEP * K,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        experts = list(range(CPU_SAMPLE_EXPERTS))
+        dt, fl = _oracle_sample(cfg, inp, experts)
+        out["cpu_baseline"] = {
+            "value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": _host_cores(), "kind": "oracle",
+            "sample": (f"float64 oracle: routing of the whole batch, then forward+backward of all "
+                       f"assignments of experts 0..{CPU_SAMPLE_EXPERTS - 1} "
+                       f"({fl / (18.0 * cfg.H * cfg.I):.0f} assignments), {dt:.1f} s")}
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

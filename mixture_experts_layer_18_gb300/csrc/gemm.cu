@@ -1,0 +1,674 @@
+// gemm.cu - persistent grouped-GEMM engine for the expert layer (sm_103a:
+// tcgen05 MMA with TMEM accumulators, TMA loads, mbarrier pipeline).
+//
+// "Accelerating dropless MoE in JAX with NVIDIA Transformer Engine",
+// "Optimisation 1: grouped GEMM": all expert GEMMs run in one launch over
+// each expert's real token count, with the counts kept on the device.  Here
+// the per-expert row ranges come from padded_offsets (a device array): every
+// 128-row tile belongs to one expert, so the tile list is derived on the GPU
+// and nothing is copied to the host.
+// "Prime Intellect releases Prime Mega MoE" (MarkTechPost), "How does the
+// fused kernel work?": SwiGLU is fused after the first expert linear and the
+// combine after the second; the backward is trainable.
+// "Prime Intellect Mega MoE" digest, "Overlapping Backward Pass": activation
+// gradients need the weights, not the weight gradients, so both kinds of tile
+// are co-scheduled in one persistent launch here (readiness counters order
+// the dX / dW13 tiles after the dH tiles they read).
+//
+// Problem kinds (A is M x K, B is K x N, all row-major in HBM):
+//   FWD1   h13 = X_perm_e W13_e, epilogue A = silu(u) * v (+ store h13)
+//          A: X_perm [rows, H] K-major;  B: W13 as [E*H, 2I] N-major.
+//          One MMA tile of N = BN covers BN/2 gate columns and the same BN/2
+//          up columns, so the activation needs no second pass.
+//   FWD2   Z = gate * (A_e W2_e)
+//          A: act [rows, I] K-major;  B: W2 as [E*I, H] N-major.
+//   BWD_D  D = dY_perm_e W2_e^T, epilogue dSwiGLU -> dh13, d(gate) partials
+//          A: dY_perm [rows, H] K-major;  B: W2 as [E*I, H] K-major.
+//   BWD_DX dXp = dh13_e W13_e^T
+//          A: dh13 [rows, 2I] K-major;  B: W13 as [E*H, 2I] K-major.
+//   DW     dW_e = S_e^T G_e over the expert's rows (K = padded rows of e)
+//          A: S [rows, M] M-major;  B: G [rows, N] N-major.
+// Every operand may instead come K-major from a transposed copy (W13^T
+// [E*2I, H], W2^T [E*H, I], S^T [M, rows], G^T [N, rows]); TF32 MMAs read
+// K-major operands only, so the fp32 mode uses those copies throughout.
+//
+// CTA layout (192 threads, one CTA per SM): warp 0 lane 0 issues TMA loads,
+// warp 1 owns TMEM and lane 0 issues tcgen05.mma, warps 2..5 run the
+// epilogue (warp w reads TMEM lanes 32*(w%4) .. +31, i.e. tile rows).  Two
+// TMEM accumulators of BN fp32 columns let the epilogue of one tile overlap
+// the MMAs of the next.  Every wait is bounded; a wait that runs out records
+// MOE_ERR_TIMEOUT, the CTA drains its copies and MMAs, frees TMEM and exits.
+#include <climits>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+enum : int { GK_FWD1 = 0, GK_FWD2 = 1, GK_BWD_D = 2, GK_BWD_DX = 3, GK_DW = 4 };
+enum : int { DEP_NONE = 0, DEP_MBLOCK = 1, DEP_EXPERT = 2 };
+
+struct GemmProblem {
+  CUtensorMap tmA;
+  CUtensorMap tmB;
+  int kind, dep, signal;
+  int a_mn, b_mn;    // operand stored M-/N-major (1) or K-major (0)
+  int M, N, K;
+  int b_expert_rows;
+  int I;
+  int nt;            // n-tiles
+  int ld_out, ld_out2, ld_aux;
+  void* out;
+  void* out2;
+  const void* aux;
+  const float* gate;
+  const int32_t* assign_of_row;
+  float* partial;
+};
+
+struct EngineParams {
+  GemmProblem prob[4];
+  int nprob;
+  int E;
+  const int32_t* padded_offsets;
+  int32_t* ready;
+  int ready_target;
+  int32_t* status;
+  unsigned long long wait_ns;
+};
+
+template <typename Elt, int BN_>
+struct Cfg {
+  static constexpr int BN = BN_;
+  static constexpr int ES = sizeof(Elt);          // 2: bf16, 4: fp32 read as tf32
+  static constexpr int BK = 128 / ES;             // k elements per pipeline stage
+  static constexpr int ATOM = 128 / ES;           // MN elements per 128-byte swizzle row
+  static constexpr int A_BYTES = 128 * 128;       // 128 rows x 128 bytes
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int ATOM_BYTES = BK * 128;     // one MN-major column block
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES_RAW = 196608 / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int KSTEPS = 4;                // MMAs per stage (32 bytes of K each)
+  static constexpr int MN_KSTEP_BYTES = (32 / ES) * 128;  // MN-major advance per MMA
+  static constexpr uint32_t FMT = ES == 2 ? 1u : 2u;      // BF16 : TF32
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*bars*/ +
+                                    (kMaxE + 1) * 4 + 64;
+};
+
+// ------------------------------------------------------------ tile decode
+struct Tile {
+  int p, kind, e, mb, m0, n0, ntile, nk, kbase;
+};
+
+template <class C>
+__device__ __forceinline__ int expert_of_row(const int* s_po, int E, int row) {
+  // last e in [0, E) with s_po[e] <= row (empty experts have equal offsets)
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_po[mid] <= row) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <class C>
+__device__ __forceinline__ Tile decode_tile(const EngineParams& P, const int* cum, const int* s_po,
+                                            int t) {
+  Tile ti;
+  int p = 0;
+  while (p + 1 < P.nprob && t >= cum[p + 1]) ++p;
+  const GemmProblem& g = P.prob[p];
+  const int lt = t - cum[p];
+  ti.p = p;
+  ti.kind = g.kind;
+  if (g.kind == GK_DW) {
+    const int mbs = (g.M + 127) / 128;
+    ti.e = lt / (mbs * g.nt);
+    const int r = lt - ti.e * mbs * g.nt;
+    ti.mb = r / g.nt;
+    ti.ntile = r - ti.mb * g.nt;
+    ti.m0 = ti.mb * 128;
+    ti.kbase = s_po[ti.e];
+    ti.nk = (s_po[ti.e + 1] - s_po[ti.e]) / C::BK;
+    ti.n0 = ti.ntile * C::BN;
+  } else {
+    ti.mb = lt / g.nt;
+    ti.ntile = lt - ti.mb * g.nt;
+    ti.m0 = ti.mb * 128;
+    ti.e = expert_of_row<C>(s_po, P.E, ti.m0);
+    ti.kbase = 0;
+    ti.nk = g.K / C::BK;
+    ti.n0 = ti.ntile * (g.kind == GK_FWD1 ? C::BN / 2 : C::BN);
+  }
+  return ti;
+}
+
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_add(int32_t* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ bool wait_counter(const int32_t* ctr, int target, const WaitCtl& c) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    if (ld_acquire(ctr) >= target) return true;
+    if (i == 0) {
+      t0 = global_ns();
+    } else if ((i & 7) == 0) {
+      if (*c.abort) return false;
+      if (global_ns() - t0 > c.limit_ns) {
+        report(c.status, MOE_ERR_TIMEOUT);
+        *c.abort = 1;
+        return false;
+      }
+    }
+    __nanosleep(256);
+  }
+}
+
+// Wait whose only exit besides success is the time limit (teardown drains).
+__device__ __forceinline__ bool wait_bar_drain(uint64_t* bar, uint32_t parity, uint64_t limit) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > limit) return false;
+  return true;
+}
+
+// ----------------------------------------------------------------- roles
+template <class C>
+__device__ void producer_role(const EngineParams& P, const int* cum, int total, const int* s_po,
+                              uint8_t* stages, uint64_t* full, uint64_t* empty,
+                              const WaitCtl& wc) {
+  int it = 0;
+  for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    const Tile ti = decode_tile<C>(P, cum, s_po, t);
+    const GemmProblem& g = P.prob[ti.p];
+    if (g.dep == DEP_MBLOCK) {
+      if (!wait_counter(P.ready + ti.mb, P.ready_target, wc)) break;
+      fence_proxy_async_global();
+    } else if (g.dep == DEP_EXPERT) {
+      bool ok = true;
+      for (int mb = s_po[ti.e] / 128; ok && mb < s_po[ti.e + 1] / 128; ++mb)
+        ok = wait_counter(P.ready + mb, P.ready_target, wc);
+      if (!ok) break;
+      fence_proxy_async_global();
+    }
+    bool ok = true;
+    for (int kb = 0; kb < ti.nk; ++kb, ++it) {
+      const int s = it % C::STAGES;
+      const uint32_t par = ((it / C::STAGES) & 1) ^ 1;
+      if (!wait_bar(&empty[s], par, wc)) { ok = false; break; }
+      uint8_t* sA = stages + s * C::STAGE_BYTES;
+      uint8_t* sB = sA + C::A_BYTES;
+      mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+      const int k0 = kb * C::BK;
+      // A operand: M-major boxes (weight gradients) or one K-major box
+      if (g.a_mn) {
+#pragma unroll
+        for (int j = 0; j < 128 / C::ATOM; ++j)
+          tma_load_2d(sA + j * C::ATOM_BYTES, &g.tmA, ti.m0 + j * C::ATOM, ti.kbase + k0, &full[s]);
+      } else {
+        tma_load_2d(sA, &g.tmA, ti.kbase + k0, ti.m0, &full[s]);
+      }
+      // B operand
+      if (!g.b_mn) {
+        const int yrow = ti.kind == GK_DW ? 0 : ti.e * g.b_expert_rows;
+        if (ti.kind == GK_FWD1) {   // gate rows then up rows, BN/2 each
+          tma_load_2d(sB, &g.tmB, ti.kbase + k0, yrow + ti.n0, &full[s]);
+          tma_load_2d(sB + (C::BN / 2) * 128, &g.tmB, ti.kbase + k0, yrow + g.I + ti.n0, &full[s]);
+        } else {
+          tma_load_2d(sB, &g.tmB, ti.kbase + k0, yrow + ti.n0, &full[s]);
+        }
+      } else {
+        const int yb = ti.kind == GK_DW ? ti.kbase + k0 : ti.e * g.b_expert_rows + k0;
+        constexpr int NA = C::BN / C::ATOM;
+#pragma unroll
+        for (int j = 0; j < NA; ++j) {
+          int x;
+          if (ti.kind == GK_FWD1) {
+            constexpr int HALF = NA / 2 > 0 ? NA / 2 : 1;  // host keeps BN >= 2*ATOM
+            x = (j / HALF) * g.I + ti.n0 + (j % HALF) * C::ATOM;
+          } else {
+            x = ti.n0 + j * C::ATOM;
+          }
+          tma_load_2d(sB + j * C::ATOM_BYTES, &g.tmB, x, yb, &full[s]);
+        }
+      }
+    }
+    if (!ok) break;
+  }
+  // Drain: the latest use of every stage must have landed before exit.
+  const int n = it < C::STAGES ? it : C::STAGES;
+  for (int q = 1; q <= n; ++q) {
+    const int u = it - q;
+    wait_bar_drain(&full[u % C::STAGES], (u / C::STAGES) & 1, wc.limit_ns);
+  }
+}
+
+template <class C>
+__device__ void mma_role(const EngineParams& P, const int* cum, int total, const int* s_po,
+                         uint8_t* stages, uint64_t* full, uint64_t* empty, uint64_t* tfull,
+                         uint64_t* tempty, uint64_t* drain, uint32_t tmem_base,
+                         const WaitCtl& wc) {
+  int it = 0, acc = 0;
+  const uint32_t sbase = smem_u32(stages);
+  for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    const Tile ti = decode_tile<C>(P, cum, s_po, t);
+    const int buf = acc & 1;
+    if (!wait_bar(&tempty[buf], ((acc >> 1) & 1) ^ 1, wc)) break;
+    tc_fence_after();
+    const uint32_t d = tmem_base + buf * C::BN;
+    if (ti.nk == 0) {
+      mbar_arrive(&tfull[buf]);
+      ++acc;
+      continue;
+    }
+    const GemmProblem& g = P.prob[ti.p];
+    const uint32_t a_mn = g.a_mn ? 1u : 0u;
+    const uint32_t b_mn = g.b_mn ? 1u : 0u;
+    const uint32_t idesc = (1u << 4) | (C::FMT << 7) | (C::FMT << 10) | (a_mn << 15) |
+                           (b_mn << 16) | ((uint32_t)(C::BN >> 3) << 17) |
+                           ((uint32_t)(128 >> 4) << 24);
+    bool ok = true;
+    for (int kb = 0; kb < ti.nk; ++kb, ++it) {
+      const int s = it % C::STAGES;
+      if (!wait_bar(&full[s], (it / C::STAGES) & 1, wc)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t aA = sbase + s * C::STAGE_BYTES;
+      const uint32_t aB = aA + C::A_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < C::KSTEPS; ++kk) {
+        const uint64_t ad = a_mn ? smem_desc_sw128(aA + kk * C::MN_KSTEP_BYTES, C::ATOM_BYTES, 1024)
+                                 : smem_desc_sw128(aA + kk * 32, 16, 1024);
+        const uint64_t bd = b_mn ? smem_desc_sw128(aB + kk * C::MN_KSTEP_BYTES, C::ATOM_BYTES, 1024)
+                                 : smem_desc_sw128(aB + kk * 32, 16, 1024);
+        if constexpr (C::ES == 2)
+          mma_f16(d, ad, bd, idesc, (kb | kk) != 0);
+        else
+          mma_tf32(d, ad, bd, idesc, (kb | kk) != 0);
+      }
+      tc_commit(&empty[s]);
+    }
+    if (!ok) break;
+    tc_commit(&tfull[buf]);
+    ++acc;
+  }
+  // Drain every MMA issued by this thread before TMEM is released.
+  tc_commit(drain);
+  wait_bar_drain(drain, 0, wc.limit_ns);
+}
+
+// ------------------------------------------------------- epilogue helpers
+template <typename Elt>
+__device__ __forceinline__ void store32(Elt* dst, const float (&v)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  if constexpr (sizeof(Elt) == 2) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      d[q] = make_uint4(pack_bf16(v[8 * q + 0], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                        pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      d[q] = make_uint4(__float_as_uint(v[4 * q + 0]), __float_as_uint(v[4 * q + 1]),
+                        __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3]));
+  }
+}
+
+template <typename Elt>
+__device__ __forceinline__ void load32(const Elt* src, float (&v)[32]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+  if constexpr (sizeof(Elt) == 2) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = s[q];
+      v[8 * q + 0] = bf16_lo(w.x); v[8 * q + 1] = bf16_hi(w.x);
+      v[8 * q + 2] = bf16_lo(w.y); v[8 * q + 3] = bf16_hi(w.y);
+      v[8 * q + 4] = bf16_lo(w.z); v[8 * q + 5] = bf16_hi(w.z);
+      v[8 * q + 6] = bf16_lo(w.w); v[8 * q + 7] = bf16_hi(w.w);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint4 w = s[q];
+      v[4 * q + 0] = __uint_as_float(w.x); v[4 * q + 1] = __uint_as_float(w.y);
+      v[4 * q + 2] = __uint_as_float(w.z); v[4 * q + 3] = __uint_as_float(w.w);
+    }
+  }
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <class C, typename Elt>
+__device__ void epilogue_role(const EngineParams& P, const int* cum, int total, const int* s_po,
+                              uint64_t* tfull, uint64_t* tempty, uint32_t tmem_base,
+                              volatile int* s_go, const WaitCtl& wc) {
+  const int q = (threadIdx.x >> 5) & 3;      // TMEM lane quarter of this warp
+  const int lane = threadIdx.x & 31;
+  const int r = q * 32 + lane;               // tile row of this thread
+  const bool leader = threadIdx.x == 64;     // first epilogue thread
+  int acc = 0;
+  for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    const Tile ti = decode_tile<C>(P, cum, s_po, t);
+    const GemmProblem& g = P.prob[ti.p];
+    const int buf = acc & 1;
+    // One thread waits; the decision is shared so all 128 threads take the
+    // same path through the named barriers below.
+    if (leader) s_go[buf] = wait_bar(&tfull[buf], (acc >> 1) & 1, wc) ? 1 : 0;
+    epi_bar();
+    if (!s_go[buf]) break;
+    tc_fence_after();
+    __syncwarp();
+    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * C::BN;
+    float v[32], w[32];
+    if (ti.kind == GK_FWD1) {
+      const int row = ti.m0 + r;
+      Elt* outA = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
+      Elt* h13 = g.out2 ? static_cast<Elt*>(g.out2) + (size_t)row * g.ld_out2 + ti.n0 : nullptr;
+#pragma unroll 1
+      for (int c = 0; c < C::BN / 2; c += 32) {
+        tmem_ld32(taddr + c, v);               // u: gate half
+        tmem_ld32(taddr + C::BN / 2 + c, w);   // v: up half
+        if (h13) {
+          store32<Elt>(h13 + c, v);
+          store32<Elt>(h13 + g.I + c, w);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = v[i] / (1.f + __expf(-v[i])) * w[i];
+        store32<Elt>(outA + c, v);
+      }
+    } else if (ti.kind == GK_FWD2) {
+      const int row = ti.m0 + r;
+      const int a = g.assign_of_row[row];
+      const float gt = a >= 0 ? g.gate[a] : 0.f;
+      Elt* out = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
+#pragma unroll 1
+      for (int c = 0; c < C::BN; c += 32) {
+        tmem_ld32(taddr + c, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= gt;
+        store32<Elt>(out + c, v);
+      }
+    } else if (ti.kind == GK_BWD_D) {
+      const int row = ti.m0 + r;
+      const int a = g.assign_of_row[row];
+      const float gt = a >= 0 ? g.gate[a] : 0.f;
+      const Elt* h13 = static_cast<const Elt*>(g.aux) + (size_t)row * g.ld_aux + ti.n0;
+      Elt* dh = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
+      float part = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < C::BN; c += 32) {
+        float D[32];
+        tmem_ld32(taddr + c, D);
+        load32<Elt>(h13 + c, v);               // u
+        load32<Elt>(h13 + g.I + c, w);         // v
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float u = v[i], vv = w[i];
+          const float sg = 1.f / (1.f + __expf(-u));
+          const float si = u * sg;
+          part += si * vv * D[i];
+          const float dA = gt * D[i];
+          v[i] = a >= 0 ? dA * vv * sg * (1.f + u * (1.f - sg)) : 0.f;   // du
+          w[i] = a >= 0 ? dA * si : 0.f;                                  // dv
+        }
+        store32<Elt>(dh + c, v);
+        store32<Elt>(dh + g.I + c, w);
+      }
+      g.partial[(size_t)row * g.nt + ti.ntile] = a >= 0 ? part : 0.f;
+    } else if (ti.kind == GK_BWD_DX) {
+      const int row = ti.m0 + r;
+      Elt* out = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
+#pragma unroll 1
+      for (int c = 0; c < C::BN; c += 32) {
+        tmem_ld32(taddr + c, v);
+        store32<Elt>(out + c, v);
+      }
+    } else {  // GK_DW
+      const bool valid = ti.m0 + r < g.M;
+      Elt* out = static_cast<Elt*>(g.out) + ((size_t)ti.e * g.M + ti.m0 + r) * g.ld_out + ti.n0;
+#pragma unroll 1
+      for (int c = 0; c < C::BN; c += 32) {
+        if (ti.nk > 0) {
+          tmem_ld32(taddr + c, v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        }
+        if (valid) store32<Elt>(out + c, v);
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(&tempty[buf]);
+    if (g.signal) {
+      // Publish this tile's rows to TMA readers in other CTAs.
+      fence_proxy_async_global();
+      __threadfence();
+      epi_bar();
+      if (leader) red_release_add(P.ready + ti.mb, 1);
+    }
+    ++acc;
+  }
+}
+
+// ----------------------------------------------------------------- kernel
+template <typename Elt, int BN>
+__global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant__ EngineParams P) {
+  using C = Cfg<Elt, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* stages = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+  int* s_go = abort_flag + 1;           // [2]
+  int* s_po = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + 256);
+
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    s_go[0] = s_go[1] = 0;
+    fence_barrier_init();
+  }
+  for (int i = threadIdx.x; i <= P.E; i += blockDim.x) s_po[i] = P.padded_offsets[i];
+  if (warp == 1) tmem_alloc(tmem_holder, C::TMEM_COLS);
+  if (threadIdx.x == 0) {
+    for (int p = 0; p < P.nprob; ++p) {
+      tma_prefetch_desc(&P.prob[p].tmA);
+      tma_prefetch_desc(&P.prob[p].tmB);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  // Tile counts per problem (derived from device offsets, no host copy).
+  int cum[5];
+  cum[0] = 0;
+  const int tpad = s_po[P.E];
+  for (int p = 0; p < 4; ++p) {
+    int n = 0;
+    if (p < P.nprob) {
+      const GemmProblem& g = P.prob[p];
+      n = g.kind == GK_DW ? P.E * ((g.M + 127) / 128) * g.nt : (tpad / 128) * g.nt;
+    }
+    cum[p + 1] = cum[p] + n;
+  }
+  const int total = cum[P.nprob];
+  const WaitCtl wc{abort_flag, P.status, P.wait_ns};
+
+  if (warp == 0) {
+    if ((threadIdx.x & 31) == 0) producer_role<C>(P, cum, total, s_po, stages, full, empty, wc);
+    __syncwarp();
+  } else if (warp == 1) {
+    if ((threadIdx.x & 31) == 0)
+      mma_role<C>(P, cum, total, s_po, stages, full, empty, tfull, tempty, drain, tmem_base, wc);
+    __syncwarp();
+  } else {
+    epilogue_role<C, Elt>(P, cum, total, s_po, tfull, tempty, tmem_base, s_go, wc);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+// ------------------------------------------------------------------- host
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major [rows, cols] tensor, 128-byte swizzled boxes of
+// box_cols x box_rows elements.
+bool make_tmap(CUtensorMap* m, const void* base, int elem_bytes, int64_t rows, int64_t cols,
+               int box_cols, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const CUtensorMapDataType dt =
+      elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                      : (elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT8);
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * elem_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int sms[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+  return sms[dev] > 0 ? sms[dev] : 1;
+}
+
+template <typename Elt, int BN>
+cudaError_t launch_typed(const EngineParams& P, int64_t tile_bound, cudaStream_t s) {
+  using C = Cfg<Elt, BN>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<Elt, BN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  int grid = sm_count();
+  if (tile_bound < grid) grid = (int)(tile_bound < 1 ? 1 : tile_bound);
+  moe_gemm_kernel<Elt, BN><<<grid, 192, C::SMEM_BYTES, s>>>(P);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st) {
+  *st = MOE_OK;
+  EngineParams P;
+  memset(&P, 0, sizeof(P));
+  P.nprob = L.nprob;
+  P.E = L.E;
+  P.padded_offsets = L.padded_offsets;
+  P.ready = L.ready;
+  P.ready_target = L.ready_target;
+  P.status = L.status;
+  P.wait_ns = L.wait_ns;
+  const int es = L.elem_bytes;
+  const int BK = 128 / es, ATOM = 128 / es;
+  int64_t tile_bound = 0;
+  const int64_t mblocks_max = (L.max_rows + 127) / 128;
+  for (int p = 0; p < L.nprob; ++p) {
+    const GemmDesc& d = L.prob[p];
+    GemmProblem& g = P.prob[p];
+    g.kind = d.kind;
+    g.a_mn = d.a_mn;
+    g.b_mn = d.b_mn;
+    g.dep = d.dep;
+    g.signal = d.signal;
+    g.M = d.M;
+    g.N = d.N;
+    g.K = d.K;
+    g.b_expert_rows = d.b_expert_rows;
+    g.I = d.I;
+    g.ld_out = d.ld_out;
+    g.ld_out2 = d.ld_out2;
+    g.ld_aux = d.ld_aux;
+    g.out = d.out;
+    g.out2 = d.out2;
+    g.aux = d.aux;
+    g.gate = d.gate;
+    g.assign_of_row = d.assign_of_row;
+    g.partial = d.partial;
+    const bool a_mn = d.a_mn != 0;
+    const bool b_mn = d.b_mn != 0;
+    if ((a_mn || b_mn) && es == 4) { *st = MOE_ERR_UNSUPPORTED; return cudaSuccess; }  // TF32: K-major only
+    if (a_mn && d.kind != GK_DW) { *st = MOE_ERR_UNSUPPORTED; return cudaSuccess; }
+    const int n_per_tile = d.kind == GK_FWD1 ? L.BN / 2 : L.BN;
+    const int n_total = d.kind == GK_FWD1 ? d.N / 2 : d.N;
+    if (n_total % n_per_tile != 0) { *st = MOE_ERR_UNSUPPORTED; return cudaSuccess; }
+    g.nt = n_total / n_per_tile;
+    bool ok = a_mn ? make_tmap(&g.tmA, d.a, es, d.a_rows, d.a_cols, ATOM, BK)
+                   : make_tmap(&g.tmA, d.a, es, d.a_rows, d.a_cols, BK, 128);
+    ok = ok && (b_mn ? make_tmap(&g.tmB, d.b, es, d.b_rows, d.b_cols, ATOM, BK)
+                     : make_tmap(&g.tmB, d.b, es, d.b_rows, d.b_cols, BK,
+                                 d.kind == GK_FWD1 ? L.BN / 2 : L.BN));
+    if (!ok) { *st = MOE_ERR_CUDA; return cudaSuccess; }
+    tile_bound += d.kind == GK_DW ? (int64_t)L.E * ((d.M + 127) / 128) * g.nt : mblocks_max * g.nt;
+  }
+  if (es == 2) {
+    switch (L.BN) {
+      case 256: return launch_typed<__nv_bfloat16, 256>(P, tile_bound, s);
+      case 128: return launch_typed<__nv_bfloat16, 128>(P, tile_bound, s);
+      case 64: return launch_typed<__nv_bfloat16, 64>(P, tile_bound, s);
+    }
+  } else if (es == 4) {
+    switch (L.BN) {
+      case 256: return launch_typed<float, 256>(P, tile_bound, s);
+      case 128: return launch_typed<float, 128>(P, tile_bound, s);
+      case 64: return launch_typed<float, 64>(P, tile_bound, s);
+    }
+  }
+  *st = MOE_ERR_UNSUPPORTED;
+  return cudaSuccess;
+}
+
+}  // namespace moe

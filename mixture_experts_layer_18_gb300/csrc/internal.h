@@ -1,0 +1,96 @@
+// internal.h - host-side launchers shared between the C-ABI layer and the
+// kernel translation units (not part of the public interface).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kAlign = 128;        // rows per expert group are padded to this
+constexpr int kRouteTokPerBlock = 128;  // tokens per block of the router
+constexpr int kMaxE = 1024;
+constexpr int kMaxTopK = 32;
+
+// route.cu
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* topk_idx,
+                         float* gate, int32_t* block_hist, int32_t* status, cudaStream_t s);
+cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int64_t max_rows,
+                           const int32_t* block_hist_in, int32_t* block_base, int32_t* counts,
+                           int32_t* offsets, int32_t* padded_offsets, int32_t* row_of_assign,
+                           int32_t* assign_of_row, int32_t* status, cudaStream_t s);
+
+// gather.cu  (elem_bytes 4: fp32 storage, 2: bf16 storage)
+cudaError_t launch_gather_rows(const void* src, void* dst, int H, int elem_bytes, int k,
+                               int n_assign, const int32_t* assign_of_row,
+                               const int32_t* padded_offsets, int E, int64_t max_rows,
+                               int32_t* status, cudaStream_t s);
+cudaError_t launch_gather_grad(const void* dY, void* dY_perm, void* dYg_perm, int H,
+                               int elem_bytes, int k, int n_assign, const int32_t* assign_of_row,
+                               const float* gate, const int32_t* padded_offsets, int E,
+                               int64_t max_rows, int32_t* status, cudaStream_t s);
+cudaError_t launch_combine(const void* src_perm, void* out, int T, int H, int elem_bytes, int k,
+                           const int32_t* row_of_assign, int64_t max_rows, int32_t* status,
+                           cudaStream_t s);
+// dst[b][c][r] = src[b][r][c] for fp32 [nb, R, C] (row pitch C) into
+// [nb, C, ld_dst] with ld_dst >= R.
+cudaError_t launch_transpose_f32(const float* src, float* dst, int nb, int64_t R, int C,
+                                 int64_t ld_dst, cudaStream_t s);
+cudaError_t launch_dgate_reduce(const float* partial, int nt, int n_assign,
+                                const int32_t* row_of_assign, int64_t max_rows, float* dgate,
+                                int32_t* status, cudaStream_t s);
+
+// quant.cu  (bf16 source; plain scale layout: [R, C/32] for axis 1,
+// [R/32, C] for axis 0)
+cudaError_t launch_quantize(const void* src, int R, int C, int ld, int axis,
+                            const int32_t* group_offsets, int G, uint8_t* q, uint8_t* scales,
+                            int32_t* status, cudaStream_t s);
+
+// gemm.cu
+struct GemmDesc {
+  int kind;                    // problem kind (gemm.cu)
+  int a_mn, b_mn;              // operand M-/N-major (1) or K-major (0)
+  int dep;                     // readiness dependency
+  int signal;                  // tiles of this problem bump readiness counters
+  const void* a;               // A source tensor
+  int64_t a_rows, a_cols;      // its 2-D extent (elements)
+  const void* b;               // B source tensor
+  int64_t b_rows, b_cols;
+  int M, N, K;                 // see GemmProblem
+  int b_expert_rows;
+  int I;
+  void* out;
+  int ld_out;
+  void* out2;
+  int ld_out2;
+  const void* aux;
+  int ld_aux;
+  const float* gate;
+  const int32_t* assign_of_row;
+  float* partial;
+};
+
+struct EngineLaunch {
+  GemmDesc prob[4];
+  int nprob;
+  int E;
+  int elem_bytes;              // 2: bf16 (kind::f16), 4: fp32 (kind::tf32)
+  int BN;                      // 64, 128 or 256
+  const int32_t* padded_offsets;
+  int64_t max_rows;
+  int32_t* ready;
+  int ready_target;
+  int32_t* status;
+  uint64_t wait_ns;
+};
+
+cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st);
+
+// debug / limits (api.cu)
+uint64_t wait_limit_ns();
+int debug_flags();
+
+}  // namespace moe

@@ -1,0 +1,478 @@
+// moe_api.cu - the C ABI declared in include/moe.h: argument checks, buffer
+// carving, and the launch sequence of each call on the caller's stream.
+#include <atomic>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+std::atomic<int> g_debug_flags{0};
+std::atomic<long long> g_wait_ns{1000000000LL};   // one second
+// one-shot timing events per call kind (forward, backward)
+std::atomic<void*> g_ev_start[3] = {nullptr, nullptr, nullptr};
+std::atomic<void*> g_ev_stop[3] = {nullptr, nullptr, nullptr};
+
+struct EventScope {   // records the pending hook's events around a launch group
+  cudaEvent_t stop = nullptr;
+  cudaStream_t s;
+  EventScope(int which, cudaStream_t st) : s(st) {
+    void* a = g_ev_start[which].exchange(nullptr);
+    void* b = g_ev_stop[which].exchange(nullptr);
+    if (a && b) {
+      cudaEventRecord(static_cast<cudaEvent_t>(a), s);
+      stop = static_cast<cudaEvent_t>(b);
+    }
+  }
+  void finish() {
+    if (stop) cudaEventRecord(stop, s);
+    stop = nullptr;
+  }
+  ~EventScope() { finish(); }
+};
+}  // namespace
+
+uint64_t wait_limit_ns() { return (uint64_t)g_wait_ns.load(); }
+int debug_flags() { return g_debug_flags.load(); }
+
+namespace {
+
+constexpr int GK_FWD1 = 0, GK_FWD2 = 1, GK_BWD_D = 2, GK_BWD_DX = 3, GK_DW = 4;
+constexpr int DEP_NONE = 0, DEP_MBLOCK = 1, DEP_EXPERT = 2;
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int elem_bytes(const moe_dims* d) { return d->mode == MOE_F32 ? 4 : 2; }
+
+bool dims_ok(const moe_dims* d) {
+  if (!d) return false;
+  if (d->T < 0 || d->E < 1 || d->E > kMaxE) return false;
+  if (d->top_k < 1 || d->top_k > kMaxTopK || d->top_k > d->E) return false;
+  if (d->H < 64 || d->H % 64 || d->I < 64 || d->I % 64) return false;
+  if (d->mode < MOE_F32 || d->mode > MOE_FP8_BWD) return false;
+  const int64_t rows = (int64_t)d->T * d->top_k + (int64_t)kAlign * d->E;
+  if (rows >= ((int64_t)1 << 31)) return false;
+  if ((int64_t)d->E * d->H * 2 * d->I >= ((int64_t)1 << 40)) return false;
+  return true;
+}
+
+int64_t max_rows(const moe_dims* d) { return (int64_t)d->T * d->top_k + (int64_t)kAlign * d->E; }
+
+bool aligned16(const void* p) { return p && ((uintptr_t)p & 15) == 0; }
+
+// Tile width of the forward gate/up GEMM: BN/2 columns of each half per tile.
+int bn_fwd1(const moe_dims* d) {
+  const int atom = 128 / elem_bytes(d);
+  for (int bn : {256, 128, 64})
+    if (bn / 2 >= atom && d->I % (bn / 2) == 0) return bn;
+  return 0;
+}
+int bn_div(int n) {
+  for (int bn : {256, 128, 64})
+    if (n % bn == 0) return bn;
+  return 0;
+}
+int bn_bwd(const moe_dims* d) {
+  for (int bn : {256, 128, 64})
+    if (d->I % bn == 0 && d->H % bn == 0) return bn;
+  return 0;
+}
+
+// fp32 mode keeps every TF32 operand K-major: the weight operands and the
+// token-axis operands of the weight-gradient GEMMs get transposed copies whose
+// row pitch is the row capacity rounded up to 32.
+int64_t ld_t(const moe_dims* d) { return (max_rows(d) + 31) / 32 * 32; }
+
+struct FwdWs {
+  size_t zg, w13t, w2t, total;
+};
+FwdWs fwd_ws(const moe_dims* d) {
+  FwdWs w;
+  const size_t rows = (size_t)max_rows(d), es = elem_bytes(d);
+  const size_t wsz = (size_t)d->E * d->H * d->I * es;
+  size_t o = 0;
+  w.zg = o; o += align256(rows * d->H * es);
+  const bool t = d->mode == MOE_F32;
+  w.w13t = o; o += t ? align256(2 * wsz) : 0;
+  w.w2t = o; o += t ? align256(wsz) : 0;
+  w.total = o;
+  return w;
+}
+
+struct BwdWs {
+  size_t dy_perm, dyg_perm, dh13, dxp, partial, ready;
+  size_t act_t, dyg_t, xp_t, dh13_t, total;
+  int nt_d;
+};
+BwdWs bwd_ws(const moe_dims* d) {
+  BwdWs w;
+  const size_t rows = (size_t)max_rows(d), es = elem_bytes(d);
+  const int bn = bn_bwd(d);
+  w.nt_d = bn ? d->I / bn : 1;
+  size_t o = 0;
+  w.dy_perm = o; o += align256(rows * d->H * es);
+  w.dyg_perm = o; o += align256(rows * d->H * es);
+  w.dh13 = o; o += align256(rows * 2 * d->I * es);
+  w.dxp = o; o += align256(rows * d->H * es);
+  w.partial = o; o += align256(rows * w.nt_d * sizeof(float));
+  w.ready = o; o += align256(((rows + 127) / 128) * sizeof(int32_t));
+  const bool t = d->mode == MOE_F32;
+  const size_t lt = (size_t)ld_t(d) * es;
+  w.act_t = o; o += t ? align256(lt * d->I) : 0;
+  w.dyg_t = o; o += t ? align256(lt * d->H) : 0;
+  w.xp_t = o; o += t ? align256(lt * d->H) : 0;
+  w.dh13_t = o; o += t ? align256(lt * 2 * d->I) : 0;
+  w.total = o;
+  return w;
+}
+
+struct RouteWs {
+  size_t hist, base, total;
+};
+RouteWs route_ws(const moe_dims* d) {
+  RouteWs w;
+  const size_t nb = (size_t)(d->T + kRouteTokPerBlock - 1) / kRouteTokPerBlock;
+  const size_t n = nb * d->E * sizeof(int32_t);
+  w.hist = 0;
+  w.base = align256(n);
+  w.total = w.base + align256(n);
+  if (w.total == 0) w.total = 256;
+  return w;
+}
+
+moe_saved_layout saved_layout(const moe_dims* d) {
+  moe_saved_layout s;
+  const size_t rows = (size_t)max_rows(d), es = elem_bytes(d);
+  size_t o = 0;
+  s.x_perm = o; o += align256(rows * d->H * es);
+  s.h13 = o; o += align256(rows * 2 * d->I * es);
+  s.act = o; o += align256(rows * d->I * es);
+  s.total = o;
+  return s;
+}
+
+// Arrays of T*top_k entries may be NULL when T == 0.
+bool route_ok(const moe_route_out* r, int T) {
+  if (!r) return false;
+  const bool tok = T == 0 || (aligned16(r->topk_idx) && aligned16(r->gate) &&
+                              aligned16(r->row_of_assign));
+  return tok && aligned16(r->counts) && aligned16(r->offsets) && aligned16(r->padded_offsets) &&
+         aligned16(r->assign_of_row);
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                                   \
+  do {                                                  \
+    cudaError_t _e = (expr);                            \
+    if (_e != cudaSuccess) return MOE_ERR_CUDA;         \
+  } while (0)
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int64_t moe_max_rows(const moe_dims* d) { return dims_ok(d) ? max_rows(d) : -1; }
+
+size_t moe_workspace_size(const moe_dims* d, int which) {
+  if (!dims_ok(d)) return 0;
+  switch (which) {
+    case MOE_WS_ROUTE: return route_ws(d).total;
+    case MOE_WS_FORWARD: return fwd_ws(d).total;
+    case MOE_WS_BACKWARD: return bwd_ws(d).total;
+  }
+  return 0;
+}
+
+moe_status moe_saved_layout_of(const moe_dims* d, moe_saved_layout* out) {
+  if (!dims_ok(d) || !out) return MOE_ERR_INVALID_ARG;
+  *out = saved_layout(d);
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_BAD_INDEX: return "index out of range";
+  }
+  return "unknown status";
+}
+
+void moe_set_gemm_events(int which, void* start, void* stop) {
+  if (which != MOE_WS_FORWARD && which != MOE_WS_BACKWARD) return;
+  g_ev_start[which].store(start && stop ? start : nullptr);
+  g_ev_stop[which].store(start && stop ? stop : nullptr);
+}
+
+void moe_set_debug(int flags, int64_t wait_limit_ns) {
+  g_debug_flags.store(flags);
+  g_wait_ns.store(wait_limit_ns > 0 ? wait_limit_ns : 1000000000LL);
+}
+
+moe_status moe_route(const moe_dims* d, const float* logits, const moe_route_out* out, void* ws,
+                     size_t ws_bytes, int32_t* dev_status, void* stream) {
+  if (!dims_ok(d) || !route_ok(out, d->T) || !aligned16(ws) || !aligned16(dev_status))
+    return MOE_ERR_INVALID_ARG;
+  if (d->T > 0 && !aligned16(logits)) return MOE_ERR_INVALID_ARG;
+  const RouteWs w = route_ws(d);
+  if (ws_bytes < w.total) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + w.hist);
+  int32_t* base = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + w.base);
+  MOE_TRY(launch_route(logits, d->T, d->E, d->top_k, out->topk_idx, out->gate, hist, dev_status, s));
+  MOE_TRY(launch_permute(out->topk_idx, d->T, d->E, d->top_k, max_rows(d), hist, base, out->counts,
+                         out->offsets, out->padded_offsets, out->row_of_assign,
+                         out->assign_of_row, dev_status, s));
+  return MOE_OK;
+}
+
+moe_status moe_forward(const moe_dims* d, const void* X, const void* W13, const void* W2,
+                       const moe_route_out* r, void* Y, void* saved, size_t saved_bytes,
+                       void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  if (!dims_ok(d) || !route_ok(r, d->T) || !aligned16(W13) || !aligned16(W2) || !aligned16(saved) ||
+      !aligned16(ws) || !aligned16(dev_status))
+    return MOE_ERR_INVALID_ARG;
+  if (d->T > 0 && (!aligned16(X) || !aligned16(Y))) return MOE_ERR_INVALID_ARG;
+  if (d->mode == MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
+  const moe_saved_layout sl = saved_layout(d);
+  const FwdWs w = fwd_ws(d);
+  if (saved_bytes < sl.total || ws_bytes < w.total) return MOE_ERR_INVALID_ARG;
+  const int bn1 = bn_fwd1(d), bn2 = bn_div(d->H);
+  if (!bn1 || !bn2) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int es = elem_bytes(d);
+  const int64_t rows = max_rows(d);
+  const int n_assign = d->T * d->top_k;
+  char* sv = static_cast<char*>(saved);
+  void* x_perm = sv + sl.x_perm;
+  void* h13 = sv + sl.h13;
+  void* act = sv + sl.act;
+  void* zg = static_cast<char*>(ws) + w.zg;
+
+  const bool f32 = d->mode == MOE_F32;
+  const void* w13_src = W13;
+  const void* w2_src = W2;
+  if (f32) {
+    float* w13t = reinterpret_cast<float*>(static_cast<char*>(ws) + w.w13t);
+    float* w2t = reinterpret_cast<float*>(static_cast<char*>(ws) + w.w2t);
+    MOE_TRY(launch_transpose_f32(static_cast<const float*>(W13), w13t, d->E, d->H, 2 * d->I, d->H, s));
+    MOE_TRY(launch_transpose_f32(static_cast<const float*>(W2), w2t, d->E, d->I, d->H, d->I, s));
+    w13_src = w13t;
+    w2_src = w2t;
+  }
+  MOE_TRY(launch_gather_rows(X, x_perm, d->H, es, d->top_k, n_assign, r->assign_of_row,
+                             r->padded_offsets, d->E, rows, dev_status, s));
+  moe_status st;
+  EventScope timing(MOE_WS_FORWARD, s);
+  EngineLaunch L;
+  memset(&L, 0, sizeof(L));
+  L.nprob = 1;
+  L.E = d->E;
+  L.elem_bytes = es;
+  L.padded_offsets = r->padded_offsets;
+  L.max_rows = rows;
+  L.status = dev_status;
+  L.wait_ns = wait_limit_ns();
+  {
+    L.BN = bn1;
+    GemmDesc& g = L.prob[0];
+    g = GemmDesc{};
+    g.kind = GK_FWD1;
+    g.a = x_perm; g.a_rows = rows; g.a_cols = d->H;
+    if (f32) {   // W13^T [E*2I, H], K-major
+      g.b = w13_src; g.b_rows = (int64_t)d->E * 2 * d->I; g.b_cols = d->H;
+      g.b_expert_rows = 2 * d->I;
+    } else {     // W13 [E*H, 2I], N-major
+      g.b_mn = 1;
+      g.b = w13_src; g.b_rows = (int64_t)d->E * d->H; g.b_cols = 2 * d->I;
+      g.b_expert_rows = d->H;
+    }
+    g.N = 2 * d->I; g.K = d->H; g.I = d->I;
+    g.out = act; g.ld_out = d->I;
+    g.out2 = d->save_for_backward ? h13 : nullptr; g.ld_out2 = 2 * d->I;
+    MOE_TRY(launch_engine(L, s, &st));
+    if (st != MOE_OK) return st;
+  }
+  {
+    L.BN = bn2;
+    GemmDesc& g = L.prob[0];
+    g = GemmDesc{};
+    g.kind = GK_FWD2;
+    g.a = act; g.a_rows = rows; g.a_cols = d->I;
+    if (f32) {   // W2^T [E*H, I], K-major
+      g.b = w2_src; g.b_rows = (int64_t)d->E * d->H; g.b_cols = d->I;
+      g.b_expert_rows = d->H;
+    } else {     // W2 [E*I, H], N-major
+      g.b_mn = 1;
+      g.b = w2_src; g.b_rows = (int64_t)d->E * d->I; g.b_cols = d->H;
+      g.b_expert_rows = d->I;
+    }
+    g.N = d->H; g.K = d->I;
+    g.out = zg; g.ld_out = d->H;
+    g.gate = r->gate; g.assign_of_row = r->assign_of_row;
+    MOE_TRY(launch_engine(L, s, &st));
+    if (st != MOE_OK) return st;
+  }
+  timing.finish();
+  MOE_TRY(launch_combine(zg, Y, d->T, d->H, es, d->top_k, r->row_of_assign, rows, dev_status, s));
+  return MOE_OK;
+}
+
+moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, const void* W2,
+                        const moe_route_out* r, const void* saved, size_t saved_bytes, void* dX,
+                        void* dW13, void* dW2, float* dgate, void* ws, size_t ws_bytes,
+                        int32_t* dev_status, void* stream) {
+  if (!dims_ok(d) || !route_ok(r, d->T) || !aligned16(W13) || !aligned16(W2) || !aligned16(saved) ||
+      !aligned16(dW13) || !aligned16(dW2) || !aligned16(ws) || !aligned16(dev_status))
+    return MOE_ERR_INVALID_ARG;
+  if (d->T > 0 && (!aligned16(dY) || !aligned16(dX) || !aligned16(dgate)))
+    return MOE_ERR_INVALID_ARG;
+  if (d->mode == MOE_MXFP8 || d->mode == MOE_FP8_BWD) return MOE_ERR_UNSUPPORTED;
+  const moe_saved_layout sl = saved_layout(d);
+  const BwdWs w = bwd_ws(d);
+  if (saved_bytes < sl.total || ws_bytes < w.total) return MOE_ERR_INVALID_ARG;
+  const int bn = bn_bwd(d);
+  if (!bn) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int es = elem_bytes(d);
+  const int64_t rows = max_rows(d);
+  const int n_assign = d->T * d->top_k;
+  const char* sv = static_cast<const char*>(saved);
+  const void* x_perm = sv + sl.x_perm;
+  const void* h13 = sv + sl.h13;
+  const void* act = sv + sl.act;
+  char* wb = static_cast<char*>(ws);
+  void* dy_perm = wb + w.dy_perm;
+  void* dyg_perm = wb + w.dyg_perm;
+  void* dh13 = wb + w.dh13;
+  void* dxp = wb + w.dxp;
+  float* partial = reinterpret_cast<float*>(wb + w.partial);
+  int32_t* ready = reinterpret_cast<int32_t*>(wb + w.ready);
+
+  MOE_TRY(launch_gather_grad(dY, dy_perm, dyg_perm, d->H, es, d->top_k, n_assign,
+                             r->assign_of_row, r->gate, r->padded_offsets, d->E, rows, dev_status,
+                             s));
+  MOE_TRY(cudaMemsetAsync(ready, 0, ((rows + 127) / 128) * sizeof(int32_t), s));
+
+  const bool f32 = d->mode == MOE_F32;
+  const int64_t lt = ld_t(d);
+  float* act_t = reinterpret_cast<float*>(wb + w.act_t);
+  float* dyg_t = reinterpret_cast<float*>(wb + w.dyg_t);
+  float* xp_t = reinterpret_cast<float*>(wb + w.xp_t);
+  float* dh13_t = reinterpret_cast<float*>(wb + w.dh13_t);
+
+  EngineLaunch L;
+  memset(&L, 0, sizeof(L));
+  L.E = d->E;
+  L.elem_bytes = es;
+  L.BN = bn;
+  L.padded_offsets = r->padded_offsets;
+  L.max_rows = rows;
+  L.ready = ready;
+  L.ready_target = (debug_flags() & MOE_DEBUG_NEVER_READY) ? 0x7fffffff : d->I / bn;
+  L.status = dev_status;
+  L.wait_ns = wait_limit_ns();
+
+  // D = dY_perm W2^T with the dSwiGLU / d(gate) epilogue (bumps readiness)
+  GemmDesc gd{};
+  gd.kind = GK_BWD_D;
+  gd.signal = 1;
+  gd.a = dy_perm; gd.a_rows = rows; gd.a_cols = d->H;
+  gd.b = W2; gd.b_rows = (int64_t)d->E * d->I; gd.b_cols = d->H;
+  gd.N = d->I; gd.K = d->H; gd.b_expert_rows = d->I; gd.I = d->I;
+  gd.out = dh13; gd.ld_out = 2 * d->I;
+  gd.aux = h13; gd.ld_aux = 2 * d->I;
+  gd.gate = r->gate; gd.assign_of_row = r->assign_of_row;
+  gd.partial = partial;
+  // dW2_e = A_e^T (gate * dY)_perm_e   (needs nothing from this launch)
+  GemmDesc gw2{};
+  gw2.kind = GK_DW;
+  gw2.M = d->I; gw2.N = d->H;
+  gw2.out = dW2; gw2.ld_out = d->H;
+  // dXp = dh13 W13^T   (waits for the m-block's D tiles)
+  GemmDesc gx{};
+  gx.kind = GK_BWD_DX;
+  gx.a = dh13; gx.a_rows = rows; gx.a_cols = 2 * d->I;
+  gx.b = W13; gx.b_rows = (int64_t)d->E * d->H; gx.b_cols = 2 * d->I;
+  gx.N = d->H; gx.K = 2 * d->I; gx.b_expert_rows = d->H;
+  gx.out = dxp; gx.ld_out = d->H;
+  // dW13_e = X_perm_e^T dh13_e   (waits for all D tiles of expert e)
+  GemmDesc gw13{};
+  gw13.kind = GK_DW;
+  gw13.M = d->H; gw13.N = 2 * d->I;
+  gw13.out = dW13; gw13.ld_out = 2 * d->I;
+
+  moe_status st;
+  EventScope timing(MOE_WS_BACKWARD, s);
+  if (!f32) {
+    gw2.a_mn = gw2.b_mn = 1;
+    gw2.a = act; gw2.a_rows = rows; gw2.a_cols = d->I;
+    gw2.b = dyg_perm; gw2.b_rows = rows; gw2.b_cols = d->H;
+    gx.dep = DEP_MBLOCK;
+    gw13.dep = DEP_EXPERT;
+    gw13.a_mn = gw13.b_mn = 1;
+    gw13.a = x_perm; gw13.a_rows = rows; gw13.a_cols = d->H;
+    gw13.b = dh13; gw13.b_rows = rows; gw13.b_cols = 2 * d->I;
+    L.nprob = 4;
+    L.prob[0] = gd;
+    L.prob[1] = gw2;
+    L.prob[2] = gx;
+    L.prob[3] = gw13;
+    MOE_TRY(launch_engine(L, s, &st));
+    if (st != MOE_OK) return st;
+  } else {
+    // TF32 reads K-major operands only: transposed token-axis copies, and the
+    // weight-gradient GEMM of W13 runs after dh13 is complete.
+    MOE_TRY(launch_transpose_f32(static_cast<const float*>(act), act_t, 1, rows, d->I, lt, s));
+    MOE_TRY(launch_transpose_f32(static_cast<const float*>(dyg_perm), dyg_t, 1, rows, d->H, lt, s));
+    MOE_TRY(launch_transpose_f32(static_cast<const float*>(x_perm), xp_t, 1, rows, d->H, lt, s));
+    gw2.a = act_t; gw2.a_rows = d->I; gw2.a_cols = lt;
+    gw2.b = dyg_t; gw2.b_rows = d->H; gw2.b_cols = lt;
+    gd.signal = 0;
+    L.nprob = 2;
+    L.prob[0] = gd;
+    L.prob[1] = gw2;
+    MOE_TRY(launch_engine(L, s, &st));
+    if (st != MOE_OK) return st;
+    MOE_TRY(launch_transpose_f32(static_cast<const float*>(dh13), dh13_t, 1, rows, 2 * d->I, lt, s));
+    gw13.a = xp_t; gw13.a_rows = d->H; gw13.a_cols = lt;
+    gw13.b = dh13_t; gw13.b_rows = 2 * d->I; gw13.b_cols = lt;
+    L.nprob = 2;
+    L.prob[0] = gx;
+    L.prob[1] = gw13;
+    MOE_TRY(launch_engine(L, s, &st));
+    if (st != MOE_OK) return st;
+  }
+  timing.finish();
+  MOE_TRY(launch_combine(dxp, dX, d->T, d->H, es, d->top_k, r->row_of_assign, rows, dev_status, s));
+  MOE_TRY(launch_dgate_reduce(partial, w.nt_d, n_assign, r->row_of_assign, rows, dgate, dev_status,
+                              s));
+  return MOE_OK;
+}
+
+moe_status moe_quantize_mxfp8(const void* src, int R, int C, int ld, int axis,
+                              const int32_t* group_offsets, int G, uint8_t* q, uint8_t* scales,
+                              int32_t* dev_status, void* stream) {
+  if (R < 0 || C < 0 || ld < C || (axis != 0 && axis != 1)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(dev_status)) return MOE_ERR_INVALID_ARG;
+  if (axis == 1 && (C % 32 != 0 || ld % 8 != 0)) return MOE_ERR_INVALID_ARG;
+  if (axis == 0 && (R % 32 != 0 || C % 2 != 0 || ld % 2 != 0)) return MOE_ERR_INVALID_ARG;
+  if (group_offsets && (axis != 0 || G < 1 || ((uintptr_t)group_offsets & 3)))
+    return MOE_ERR_INVALID_ARG;
+  if ((int64_t)R * C > 0 && (!aligned16(src) || !aligned16(q) || !scales))
+    return MOE_ERR_INVALID_ARG;
+  MOE_TRY(launch_quantize(src, R, C, ld, axis, group_offsets, G, q, scales, dev_status,
+                          static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+}  // extern "C"

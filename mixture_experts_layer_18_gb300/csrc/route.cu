@@ -1,0 +1,239 @@
+// route.cu - top-k router and permutation builder.
+//
+// Router: "Prime Intellect releases Prime Mega MoE" (MarkTechPost), "In
+// brief": each token goes to its top-8 of 128 experts.  Gates are the
+// softmax over all experts renormalised over the chosen ones, which equals
+// exp(l_j - m) / sum_{i in top-k} exp(l_i - m) with m the largest logit.
+// Permutation: "Accelerating dropless MoE in JAX with NVIDIA Transformer
+// Engine", 02 (dropless: every assignment kept, ragged per-expert groups)
+// and "Optimisation 2" (dispatch reorders token copies by expert locally).
+// Storage groups are padded to 128 rows so that every 128-row GEMM tile
+// belongs to one expert; the logical counts stay unpadded.
+#include <climits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRouteThreads = 256;                      // 8 warps
+constexpr int kTokPerWarp = kRouteTokPerBlock / (kRouteThreads / 32);
+
+// One warp per token.  Lane l holds logits l, l+32, l+64, ... in registers.
+// k rounds of a warp arg-max pick the largest remaining logit, ties to the
+// lower expert index (a total order for NaN-free input).  Slot j of the
+// result is the j-th pick.  Also builds this block's expert histogram.
+template <int VPL>
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,
+    float* __restrict__ gate, int32_t* __restrict__ block_hist, int nb) {
+  __shared__ int hist[kMaxE];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = 0; i < kTokPerWarp; ++i) {
+    const int t = blockIdx.x * kRouteTokPerBlock + warp * kTokPerWarp + i;
+    if (t >= T) break;
+    const float* row = logits + (size_t)t * E;
+    float v[VPL];
+    uint32_t taken = 0;  // bit q: element q*32+lane chosen already or absent
+#pragma unroll
+    for (int q = 0; q < VPL; ++q) {
+      const int e = q * 32 + lane;
+      v[q] = e < E ? __ldg(row + e) : 0.f;
+      if (e >= E) taken |= 1u << q;
+    }
+    float sel_v = 0.f;
+    int sel_e = 0;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int be = INT_MAX;
+#pragma unroll
+      for (int q = 0; q < VPL; ++q) {
+        const int e = q * 32 + lane;
+        if (!((taken >> q) & 1u) && (v[q] > bv || (v[q] == bv && e < be))) {
+          bv = v[q];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        if (ov > bv || (ov == bv && oe < be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (lane == j) {
+        sel_v = bv;
+        sel_e = be;
+      }
+    }
+    const float m = __shfl_sync(0xffffffffu, sel_v, 0);
+    const float w = lane < k ? expf(sel_v - m) : 0.f;
+    float sum = w;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane < k) {
+      topk_idx[(size_t)t * k + lane] = sel_e;
+      gate[(size_t)t * k + lane] = w / sum;
+      atomicAdd(&hist[sel_e], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) block_hist[(size_t)e * nb + blockIdx.x] = hist[e];
+}
+
+// Single block: per-expert totals and the per-(expert, block) exclusive
+// bases, then the exclusive scans over experts (logical and padded).
+__global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ block_hist, int nb,
+                                                    int E, int32_t* __restrict__ block_base,
+                                                    int32_t* __restrict__ counts,
+                                                    int32_t* __restrict__ offsets,
+                                                    int32_t* __restrict__ padded_offsets) {
+  __shared__ int s_cnt[kMaxE];
+  __shared__ int s_pad[kMaxE + 1];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int b = 0; b < nb; ++b) {
+      const int c = block_hist[(size_t)e * nb + b];
+      block_base[(size_t)e * nb + b] = run;
+      run += c;
+    }
+    s_cnt[e] = run;
+    s_pad[e] = (run + kAlign - 1) / kAlign * kAlign;
+    counts[e] = run;
+  }
+  __syncthreads();
+  // E <= 1024: a warp-parallel scan over 32-expert chunks.
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry_o = 0, carry_p = 0;
+    for (int c0 = 0; c0 < E; c0 += 32) {
+      const int e = c0 + lane;
+      int o = e < E ? s_cnt[e] : 0;
+      int p = e < E ? s_pad[e] : 0;
+      // inclusive warp scans
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int yo = __shfl_up_sync(0xffffffffu, o, off);
+        const int yp = __shfl_up_sync(0xffffffffu, p, off);
+        if (lane >= off) {
+          o += yo;
+          p += yp;
+        }
+      }
+      if (e < E) {
+        offsets[e] = carry_o + o - s_cnt[e];
+        padded_offsets[e] = carry_p + p - s_pad[e];
+      }
+      carry_o += __shfl_sync(0xffffffffu, o, 31);
+      carry_p += __shfl_sync(0xffffffffu, p, 31);
+    }
+    if (lane == 0) {
+      offsets[E] = carry_o;
+      padded_offsets[E] = carry_p;
+    }
+  }
+}
+
+// Blocks [0, nb): stable scatter of this block's assignments (the same
+// assignment ranges as the router blocks).  Within a 256-assignment round,
+// lanes of a warp with equal experts are ranked by lane (match_any), warps
+// take their bases from the running per-expert cursor in warp order, so the
+// rank of an assignment inside its expert follows ascending a.
+// Blocks [nb, gridDim): mark pad rows and rows past padded_offsets[E] with -1.
+__global__ void __launch_bounds__(256) scatter_kernel(
+    const int32_t* __restrict__ topk_idx, int n_assign, int E, int k, int nb,
+    const int32_t* __restrict__ block_base, const int32_t* __restrict__ counts,
+    const int32_t* __restrict__ padded_offsets, int32_t* __restrict__ row_of_assign,
+    int32_t* __restrict__ assign_of_row, int64_t max_rows, int32_t* status) {
+  __shared__ int run[kMaxE];
+  __shared__ int s_base[8][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if ((int)blockIdx.x >= nb) {
+    const int pb = blockIdx.x - nb, npb = gridDim.x - nb;
+    for (int e = pb; e < E; e += npb) {
+      const int r1 = padded_offsets[e + 1];
+      for (int r = padded_offsets[e] + counts[e] + threadIdx.x; r < r1; r += blockDim.x)
+        assign_of_row[r] = -1;
+    }
+    for (int64_t r = (int64_t)padded_offsets[E] + (int64_t)pb * blockDim.x + threadIdx.x;
+         r < max_rows; r += (int64_t)npb * blockDim.x)
+      assign_of_row[r] = -1;
+    return;
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    run[e] = padded_offsets[e] + block_base[(size_t)e * nb + blockIdx.x];
+  __syncthreads();
+  const int chunk = kRouteTokPerBlock * k;
+  const int a0 = blockIdx.x * chunk;
+  const int a1 = min(n_assign, a0 + chunk);
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int base = a0; base < a1; base += blockDim.x) {
+    const int a = base + threadIdx.x;
+    int e = a < a1 ? topk_idx[a] : -1;
+    if (e >= E || (a < a1 && e < 0)) {
+      report(status, MOE_ERR_BAD_INDEX);
+      e = -1;
+    }
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(same & lt_mask);
+    const int leader = __ffs(same) - 1;
+    for (int w = 0; w < 8; ++w) {
+      if (warp == w && lane == leader && e >= 0) {
+        s_base[w][lane] = run[e];
+        run[e] += __popc(same);
+      }
+      __syncthreads();
+    }
+    if (e >= 0) {
+      const int row = s_base[warp][leader] + rank;
+      row_of_assign[a] = row;
+      assign_of_row[row] = a;
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* topk_idx,
+                         float* gate, int32_t* block_hist, int32_t* /*status*/,
+                         cudaStream_t s) {
+  const int nb = (T + kRouteTokPerBlock - 1) / kRouteTokPerBlock;
+  if (nb == 0) return cudaSuccess;
+  const int vpl = (E + 31) / 32;
+  if (vpl <= 1)
+    route_kernel<1><<<nb, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
+  else if (vpl <= 4)
+    route_kernel<4><<<nb, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
+  else if (vpl <= 8)
+    route_kernel<8><<<nb, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
+  else if (vpl <= 16)
+    route_kernel<16><<<nb, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
+  else
+    route_kernel<32><<<nb, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int64_t max_rows,
+                           const int32_t* block_hist, int32_t* block_base, int32_t* counts,
+                           int32_t* offsets, int32_t* padded_offsets, int32_t* row_of_assign,
+                           int32_t* assign_of_row, int32_t* status, cudaStream_t s) {
+  const int nb = (T + kRouteTokPerBlock - 1) / kRouteTokPerBlock;
+  scan_kernel<<<1, 1024, 0, s>>>(block_hist, nb, E, block_base, counts, offsets, padded_offsets);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const int pad_blocks = 64;
+  scatter_kernel<<<nb + pad_blocks, 256, 0, s>>>(topk_idx, T * k, E, k, nb, block_base, counts,
+                                                 padded_offsets, row_of_assign, assign_of_row,
+                                                 max_rows, status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

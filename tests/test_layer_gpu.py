@@ -1,0 +1,168 @@
+"""Forward and backward of the expert layer on the GPU (through the C ABI)
+vs the float64 oracle on the same seeded inputs.
+
+Small shapes are compared element by element over every output; the full
+workload shapes (Qwen3-30B-A3B / 235B-A22B layers, uniform and Zipf-skewed
+routing) are compared on sampled tokens and experts, in the launch
+configuration the benchmark times."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as O
+from workloads import CONFIGS, MoEConfig, make_inputs
+
+from _common import TOL_BF16, F32View, rel_err, to_device, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(cfg: MoEConfig, inp, mode=None):
+    import torch
+    from mixture_experts_layer_18_gb300.layer import MoELayer
+    mode = mode or ("f32" if cfg.dtype == "f32" else "bf16")
+    L = MoELayer(cfg.T, cfg.H, cfg.E, cfg.I, cfg.k, mode=mode)
+    io = L.empty_io()
+    dev = {k: to_device(v) for k, v in inp.items()}
+    L.route(dev["logits"])
+    L.forward(dev["X"], dev["W13"], dev["W2"], io["Y"])
+    L.backward(dev["dY"], dev["W13"], dev["W2"], io["dX"], io["dW13"], io["dW2"], io["dgate"])
+    torch.cuda.synchronize()
+    assert L.device_status() == 0
+    return L, io
+
+
+def _oracle_inputs(inp):
+    return {k: (F32View(v) if k != "logits" else v) for k, v in inp.items()}
+
+
+def _check_small(cfg, seed=0, mode=None, tol=TOL_BF16):
+    inp = make_inputs(cfg, seed)
+    L, io = _run(cfg, inp, mode)
+    oi = _oracle_inputs(inp)
+    idx, gate = O.route(inp["logits"], cfg.k)
+    Y, saved = O.forward(oi["X"], oi["W13"], oi["W2"], idx, gate, keep=True)
+    g = O.backward(oi["X"], oi["W13"], oi["W2"], idx, gate, oi["dY"])
+    # intermediates: gathered rows, h13 and the activation, row by row
+    roa = L.row_of_assign.cpu().numpy()
+    xp, h13, act = to_f64(L.x_perm), to_f64(L.h13), to_f64(L.act)
+    X = np.asarray(oi["X"], np.float64)
+    for e, s in saved.items():
+        rows = roa[s["a"]]
+        assert np.array_equal(xp[rows], X[s["a"] // cfg.k]), e
+        assert rel_err(h13[rows], s["h"]) <= tol, ("h13", e)
+        assert rel_err(act[rows], s["A"]) <= tol, ("act", e)
+    pad = L.assign_of_row.cpu().numpy()[: int(L.padded_offsets[-1])] < 0
+    assert (xp[: len(pad)][pad] == 0).all()
+    errs = {"Y": rel_err(to_f64(io["Y"]), Y), "dX": rel_err(to_f64(io["dX"]), g["dX"]),
+            "dW13": rel_err(to_f64(io["dW13"]), g["dW13"]),
+            "dW2": rel_err(to_f64(io["dW2"]), g["dW2"]),
+            "dgate": rel_err(to_f64(io["dgate"]), g["dgate"])}
+    for k, v in errs.items():
+        assert v <= tol, (k, v, errs)
+    return errs
+
+
+def test_tiny_fp32_full():
+    _check_small(CONFIGS["tiny"])
+
+
+SMALL = {
+    "bf16_a": MoEConfig("bf16_a", 300, 256, 8, 2, 128, "bf16"),
+    "bf16_b": MoEConfig("bf16_b", 1024, 512, 16, 4, 256, "bf16"),
+    "bf16_odd_I": MoEConfig("bf16_odd_I", 500, 128, 16, 4, 192, "bf16"),
+    "bf16_k1": MoEConfig("bf16_k1", 257, 192, 4, 1, 64, "bf16"),
+    "f32_wide": MoEConfig("f32_wide", 200, 256, 8, 4, 128, "f32", modes=("f32",)),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_shapes_full(name):
+    _check_small(SMALL[name])
+
+
+def test_skewed_routing_with_empty_experts():
+    cfg = MoEConfig("skew_small", 600, 256, 32, 4, 128, "bf16", skew=True)
+    inp = make_inputs(cfg)
+    idx, _ = O.route(inp["logits"], cfg.k)
+    counts = np.bincount(idx.reshape(-1), minlength=cfg.E)
+    assert (counts == 0).sum() >= 8 and counts.max() > 4 * counts[counts > 0].min()
+    _check_small(cfg)
+
+
+def test_empty_batch_gives_zero_weight_gradients():
+    import torch
+    from mixture_experts_layer_18_gb300.layer import MoELayer
+    L = MoELayer(0, 128, 4, 64, 2, mode="bf16")
+    io = L.empty_io()
+    W13 = torch.randn(4, 128, 128, device="cuda").bfloat16()
+    W2 = torch.randn(4, 64, 128, device="cuda").bfloat16()
+    io["dW13"].fill_(1.0)
+    io["dW2"].fill_(1.0)
+    L.route(torch.empty((0, 4), device="cuda"))
+    L.forward(None, W13, W2, io["Y"])
+    L.backward(None, W13, W2, io["dX"], io["dW13"], io["dW2"], io["dgate"])
+    torch.cuda.synchronize()
+    assert L.device_status() == 0
+    assert (io["dW13"] == 0).all() and (io["dW2"] == 0).all()
+
+
+def test_forward_backward_deterministic():
+    import torch
+    cfg = SMALL["bf16_b"]
+    inp = make_inputs(cfg, 3)
+    _, a = _run(cfg, inp)
+    _, b = _run(cfg, inp)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+# ------------------------------------------------------------ full sizes
+def _sample_experts(counts, rng):
+    nz = np.nonzero(counts)[0]
+    ex = {int(np.argmax(counts)), int(nz[np.argmin(counts[nz])]), int(rng.choice(nz))}
+    zero = np.nonzero(counts == 0)[0]
+    if zero.size:
+        ex.add(int(zero[0]))
+    return sorted(ex)
+
+
+@pytest.mark.parametrize("name", ["30b", "30b_zipf", "235b"])
+def test_full_size_sampled(name):
+    cfg = CONFIGS[name]
+    inp = make_inputs(cfg)
+    L, io = _run(cfg, inp)
+    oi = _oracle_inputs(inp)
+    idx, gate = O.route(inp["logits"], cfg.k)
+    counts = np.bincount(idx.reshape(-1), minlength=cfg.E)
+    assert np.array_equal(L.counts.cpu().numpy(), counts)
+    rng = np.random.default_rng(1)
+    tokens = np.sort(rng.choice(cfg.T, 256, replace=False))
+    experts = _sample_experts(counts, rng)
+    Y = O.forward(oi["X"], oi["W13"], oi["W2"], idx, gate, tokens=tokens)
+    g = O.backward(oi["X"], oi["W13"], oi["W2"], idx, gate, oi["dY"], tokens=tokens,
+                   experts=experts)
+    errs = {
+        "Y": rel_err(to_f64(io["Y"][tokens]), Y),
+        "dX": rel_err(to_f64(io["dX"][tokens]), g["dX"]),
+        "dgate": rel_err(to_f64(io["dgate"][tokens]), g["dgate"]),
+    }
+    for i, e in enumerate(experts):
+        if counts[e] == 0:
+            assert (to_f64(io["dW13"][e]) == 0).all() and (to_f64(io["dW2"][e]) == 0).all()
+            continue
+        errs[f"dW13[{e}]"] = rel_err(to_f64(io["dW13"][e]), g["dW13"][i])
+        errs[f"dW2[{e}]"] = rel_err(to_f64(io["dW2"][e]), g["dW2"][i])
+    for k, v in errs.items():
+        assert v <= TOL_BF16, (k, v, errs)
+    # properties that hold everywhere: finite outputs, zero grads for empty experts
+    for k in ("Y", "dX", "dgate"):
+        assert torch_finite(io[k])
+    for e in np.nonzero(counts == 0)[0]:
+        assert (to_f64(io["dW13"][int(e)]) == 0).all()
+
+
+def torch_finite(t):
+    import torch
+    return bool(torch.isfinite(t).all().item())
