@@ -48,7 +48,23 @@ def _args():
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--workload", default="235b", choices=[k for k in CONFIGS if k != "tiny"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    # smaller variants of the workload, for profiler captures
+    p.add_argument("--tokens", type=int, default=None, help="override T")
+    p.add_argument("--experts", type=int, default=None, help="override E")
     return p.parse_args()
+
+
+def _config(args):
+    import dataclasses
+    cfg = CONFIGS[args.workload]
+    kw = {}
+    if args.tokens:
+        kw["T"] = args.tokens
+    if args.experts:
+        kw["E"] = args.experts
+    if kw:
+        cfg = dataclasses.replace(cfg, name=cfg.name + "-variant", **kw)
+    return cfg
 
 
 def _peaks():
@@ -183,7 +199,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    cfg = CONFIGS[args.workload]
+    cfg = _config(args)
     inp = make_inputs(cfg)
     times, flops = [], []
     for i in range(args.warmup + args.steps):
@@ -223,7 +239,7 @@ def run_gpu(args):
     if world > 1:
         dist.init_process_group(backend="nccl")
     torch.cuda.set_device(local)
-    cfg = CONFIGS[args.workload]
+    cfg = _config(args)
     inp = make_inputs(cfg, seed=rank)
 
     def dev(a):
