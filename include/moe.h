@@ -134,6 +134,25 @@ moe_status moe_route(const moe_dims* dims, const float* logits,
                      const moe_route_out* out, void* ws, size_t ws_bytes,
                      int32_t* dev_status, void* stream);
 
+/* moe_route without a workspace argument, for callers that cannot allocate
+ * device memory.  The pages have no counterpart: it exists for integrations
+ * such as plugins inside a host framework that owns every device allocation
+ * and exposes no workspace hook, or latency-critical loops that must not call
+ * cudaMalloc (which can synchronise the device) after start-up.  Results are
+ * identical to moe_route.
+ *   Scratch: a library-owned device array of 512 KiB (131072 int32) that
+ *   every GPU which loads the library holds until process exit.  Requires
+ *   2 * E * ceil(T / 128) <= 131072, else MOE_ERR_INVALID_ARG (no launch).
+ *   The first call on a device looks up the array's device address with that
+ *   device current (no allocation); make that first call before any stream
+ *   capture.  The library calls no cudaMalloc / cudaFree here.
+ *   All calls share the one array: calls whose work can overlap on the GPU
+ *   (different streams, or different host threads) race and must be ordered
+ *   by the caller.  Each call writes every scratch entry it reads. */
+moe_status moe_route_noalloc(const moe_dims* dims, const float* logits,
+                             const moe_route_out* out, int32_t* dev_status,
+                             void* stream);
+
 /* Forward of the expert layer ([MM] "How does the fused kernel work?";
  * [TE] "Optimisation 1" and "Optimisation 2"):
  *   X_perm = rows of X in expert-major order (pad rows 0)

@@ -476,3 +476,66 @@ moe_status moe_quantize_mxfp8(const void* src, int R, int C, int ld, int axis,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// moe_route_noalloc: the router and permutation builder for callers that
+// cannot allocate device memory (see include/moe.h).  Its scratch (the
+// per-block expert histograms and their exclusive bases, 2 * E * ceil(T/128)
+// int32) lives in one file-scope device array instead of a caller workspace.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr int64_t kNoAllocRouteInts = 131072;   // 512 KiB of int32 scratch
+__device__ __align__(256) int32_t g_route_scratch[kNoAllocRouteInts];
+
+// In host code g_route_scratch names a host-side stand-in, not the device
+// array, so its device address is looked up once per device (with that device
+// current) and cached.
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+int32_t* g_scratch_ptr[kMaxDevices] = {};
+
+cudaError_t route_scratch_ptr(int32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_route_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_route_noalloc(const moe_dims* d, const float* logits,
+                                        const moe_route_out* out, int32_t* dev_status,
+                                        void* stream) {
+  using namespace moe;
+  if (!dims_ok(d) || !route_ok(out, d->T) || !aligned16(dev_status)) return MOE_ERR_INVALID_ARG;
+  if (d->T > 0 && !aligned16(logits)) return MOE_ERR_INVALID_ARG;
+  const int64_t nb = ((int64_t)d->T + kRouteTokPerBlock - 1) / kRouteTokPerBlock;
+  if (2 * nb * d->E > kNoAllocRouteInts) return MOE_ERR_INVALID_ARG;   // scratch too small
+  int32_t* scratch = nullptr;
+  if (route_scratch_ptr(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  // Every scratch entry read below is first written by the same call (the
+  // router writes all E x nb histogram entries, the scan all bases), so no
+  // clearing is needed.
+  int32_t* hist = scratch;
+  int32_t* base = scratch + nb * d->E;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MOE_TRY(launch_route(logits, d->T, d->E, d->top_k, out->topk_idx, out->gate, hist, dev_status, s));
+  MOE_TRY(launch_permute(out->topk_idx, d->T, d->E, d->top_k, max_rows(d), hist, base, out->counts,
+                         out->offsets, out->padded_offsets, out->row_of_assign,
+                         out->assign_of_row, dev_status, s));
+  return MOE_OK;
+}
