@@ -214,8 +214,10 @@ const char* moe_status_string(moe_status s);
  * (0 restores the default of one second).  Flag MOE_DEBUG_NEVER_READY makes
  * the co-scheduled backward wait on a readiness counter that is never
  * bumped, so the bounded wait runs out and MOE_ERR_TIMEOUT is reported.
+ * Flag MOE_DEBUG_SINGLE_CTA runs the bf16 GEMMs with single-CTA 128-row
+ * tiles instead of 256-row tiles over an SM pair (for A/B comparison).
  * Process-wide; not thread-safe against concurrent calls. */
-enum { MOE_DEBUG_NEVER_READY = 1 };
+enum { MOE_DEBUG_NEVER_READY = 1, MOE_DEBUG_SINGLE_CTA = 2 };
 void moe_set_debug(int flags, int64_t wait_limit_ns);
 
 /* Timing hook for kernel-level measurement.  `start` and `stop` are

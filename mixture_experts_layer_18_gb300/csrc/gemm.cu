@@ -34,7 +34,12 @@
 //
 // CTA layout (192 threads, one CTA per SM): warp 0 lane 0 issues TMA loads,
 // warp 1 owns TMEM and lane 0 issues tcgen05.mma, warps 2..5 run the
-// epilogue (warp w reads TMEM lanes 32*(w%4) .. +31, i.e. tile rows).  Two
+// epilogue (warp w reads TMEM lanes 32*(w%4) .. +31, i.e. tile rows).
+// bf16 problems run on SM pairs (clusters of 2, cta_group::2): one 256-row
+// tile per pair, each CTA staging its 128 rows of A and half of B, so a
+// pipeline stage is 32 KB per CTA (6 stages) instead of 48 KB (4 stages) and
+// each SM's shared-memory traffic per MMA drops by a third.  The leader CTA
+// issues the MMAs; its commits signal both CTAs' barriers.  Two
 // TMEM accumulators of BN fp32 columns let the epilogue of one tile overlap
 // the MMAs of the next.  Every wait is bounded; a wait that runs out records
 // MOE_ERR_TIMEOUT, the CTA drains its copies and MMAs, frees TMEM and exits.
@@ -65,6 +70,7 @@ struct GemmProblem {
   const void* aux;
   const float* gate;
   const int32_t* assign_of_row;
+  int n_assign;      // valid assignment indices are [0, n_assign)
   float* partial;
 };
 
@@ -79,14 +85,16 @@ struct EngineParams {
   unsigned long long wait_ns;
 };
 
-template <typename Elt, int BN_>
+template <typename Elt, int BN_, int PAIR_>
 struct Cfg {
-  static constexpr int BN = BN_;
+  static constexpr int PAIR = PAIR_;              // CTAs per MMA tile (1, or 2 = SM pair)
+  static constexpr int BN = BN_;                  // MMA N = accumulator columns
+  static constexpr int BNL = BN / PAIR;           // B columns staged by each CTA
   static constexpr int ES = sizeof(Elt);          // 2: bf16, 4: fp32 read as tf32
   static constexpr int BK = 128 / ES;             // k elements per pipeline stage
   static constexpr int ATOM = 128 / ES;           // MN elements per 128-byte swizzle row
   static constexpr int A_BYTES = 128 * 128;       // 128 rows x 128 bytes
-  static constexpr int B_BYTES = BN * 128;
+  static constexpr int B_BYTES = BNL * 128;
   static constexpr int ATOM_BYTES = BK * 128;     // one MN-major column block
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES_RAW = 196608 / STAGE_BYTES;
@@ -96,28 +104,30 @@ struct Cfg {
   static constexpr int MN_KSTEP_BYTES = (32 / ES) * 128;  // MN-major advance per MMA
   static constexpr uint32_t FMT = ES == 2 ? 1u : 2u;      // BF16 : TF32
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*bars*/ +
-                                    (kMaxE + 1) * 4 + 64;
+                                    2 * (kMaxE + 1) * 4 + 64;
 };
 
 // ------------------------------------------------------------ tile decode
+// A tile is 128 x BN per CTA.  With PAIR == 2 the two CTAs of a cluster
+// compute one 256 x BN tile: CTA rank r owns rows [128 r, 128 r + 128).
 struct Tile {
   int p, kind, e, mb, m0, n0, ntile, nk, kbase;
+  bool valid;   // this CTA's 128 rows belong to the tile's expert (or M)
 };
 
-template <class C>
-__device__ __forceinline__ int expert_of_row(const int* s_po, int E, int row) {
-  // last e in [0, E) with s_po[e] <= row (empty experts have equal offsets)
+// last e in [0, E) with arr[e] <= v (entries of empty experts repeat)
+__device__ __forceinline__ int last_le(const int* arr, int E, int v) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (s_po[mid] <= row) lo = mid; else hi = mid - 1;
+    if (arr[mid] <= v) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
 
 template <class C>
 __device__ __forceinline__ Tile decode_tile(const EngineParams& P, const int* cum, const int* s_po,
-                                            int t) {
+                                            const int* s_pt, int t, int rank) {
   Tile ti;
   int p = 0;
   while (p + 1 < P.nprob && t >= cum[p + 1]) ++p;
@@ -126,20 +136,30 @@ __device__ __forceinline__ Tile decode_tile(const EngineParams& P, const int* cu
   ti.p = p;
   ti.kind = g.kind;
   if (g.kind == GK_DW) {
-    const int mbs = (g.M + 127) / 128;
-    ti.e = lt / (mbs * g.nt);
-    const int r = lt - ti.e * mbs * g.nt;
-    ti.mb = r / g.nt;
-    ti.ntile = r - ti.mb * g.nt;
+    const int mslots = ((g.M + 127) / 128 + C::PAIR - 1) / C::PAIR;
+    ti.e = lt / (mslots * g.nt);
+    const int r = lt - ti.e * mslots * g.nt;
+    const int i = r / g.nt;
+    ti.ntile = r - i * g.nt;
+    ti.mb = i * C::PAIR + rank;
     ti.m0 = ti.mb * 128;
+    ti.valid = ti.m0 < g.M;
     ti.kbase = s_po[ti.e];
     ti.nk = (s_po[ti.e + 1] - s_po[ti.e]) / C::BK;
     ti.n0 = ti.ntile * C::BN;
   } else {
-    ti.mb = lt / g.nt;
-    ti.ntile = lt - ti.mb * g.nt;
+    const int q = lt / g.nt;
+    ti.ntile = lt - q * g.nt;
+    if (C::PAIR == 1) {
+      ti.mb = q;
+      ti.e = last_le(s_po, P.E, q * 128);
+      ti.valid = true;
+    } else {
+      ti.e = last_le(s_pt, P.E, q);
+      ti.mb = s_po[ti.e] / 128 + 2 * (q - s_pt[ti.e]) + rank;
+      ti.valid = ti.mb < s_po[ti.e + 1] / 128;
+    }
     ti.m0 = ti.mb * 128;
-    ti.e = expert_of_row<C>(s_po, P.E, ti.m0);
     ti.kbase = 0;
     ti.nk = g.K / C::BK;
     ti.n0 = ti.ntile * (g.kind == GK_FWD1 ? C::BN / 2 : C::BN);
@@ -175,6 +195,31 @@ __device__ __forceinline__ bool wait_counter(const int32_t* ctr, int target, con
   }
 }
 
+// Bounded wait on a barrier that also receives arrivals from the peer CTA.
+__device__ __forceinline__ bool wait_bar_cluster(uint64_t* bar, uint32_t parity, const WaitCtl& c) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*c.abort) return false;
+      if (global_ns() - t0 > c.limit_ns) {
+        report(c.status, MOE_ERR_TIMEOUT);
+        *c.abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Barriers of a CTA pair also receive arrivals / byte counts from the peer
+// CTA and from 2-CTA commits, so pair kernels wait with cluster scope.
+template <class C>
+__device__ __forceinline__ bool wait_bar_p(uint64_t* bar, uint32_t parity, const WaitCtl& c) {
+  if constexpr (C::PAIR == 2) return wait_bar_cluster(bar, parity, c);
+  else return wait_bar(bar, parity, c);
+}
+
 // Wait whose only exit besides success is the time limit (teardown drains).
 __device__ __forceinline__ bool wait_bar_drain(uint64_t* bar, uint32_t parity, uint64_t limit) {
   const uint64_t t0 = global_ns();
@@ -183,17 +228,30 @@ __device__ __forceinline__ bool wait_bar_drain(uint64_t* bar, uint32_t parity, u
   return true;
 }
 
+template <class C>
+__device__ __forceinline__ void tma_load(void* dst, const CUtensorMap* m, int x, int y,
+                                         uint64_t* bar, uint32_t bar_cluster) {
+  if constexpr (C::PAIR == 2)
+    tma_load_2d_pair(dst, m, x, y, bar_cluster);
+  else
+    tma_load_2d(dst, m, x, y, bar);
+}
+
 // ----------------------------------------------------------------- roles
+// Producer (one thread per CTA).  With PAIR == 2 both CTAs load their own A
+// rows and their half of B into their own shared memory, and both signal the
+// leader CTA's full barrier, which the leader arms with the pair's bytes.
 template <class C>
 __device__ void producer_role(const EngineParams& P, const int* cum, int total, const int* s_po,
-                              uint8_t* stages, uint64_t* full, uint64_t* empty,
-                              const WaitCtl& wc) {
+                              const int* s_pt, int rank, uint8_t* stages, uint64_t* full,
+                              uint64_t* empty, const WaitCtl& wc) {
   int it = 0;
-  for (int t = blockIdx.x; t < total; t += gridDim.x) {
-    const Tile ti = decode_tile<C>(P, cum, s_po, t);
+  const int cl = blockIdx.x / C::PAIR, ncl = gridDim.x / C::PAIR;
+  for (int t = cl; t < total; t += ncl) {
+    const Tile ti = decode_tile<C>(P, cum, s_po, s_pt, t, rank);
     const GemmProblem& g = P.prob[ti.p];
     if (g.dep == DEP_MBLOCK) {
-      if (!wait_counter(P.ready + ti.mb, P.ready_target, wc)) break;
+      if (ti.valid && !wait_counter(P.ready + ti.mb, P.ready_target, wc)) break;
       fence_proxy_async_global();
     } else if (g.dep == DEP_EXPERT) {
       bool ok = true;
@@ -202,73 +260,87 @@ __device__ void producer_role(const EngineParams& P, const int* cum, int total, 
       if (!ok) break;
       fence_proxy_async_global();
     }
+    // B column segments staged by this CTA: (first column or row, count)
+    int seg0, seg1 = -1, seglen;
+    if (ti.kind == GK_FWD1) {
+      seglen = C::BN / 2;
+      if (C::PAIR == 1) {
+        seg0 = ti.n0;
+        seg1 = g.I + ti.n0;
+      } else {
+        seg0 = rank ? g.I + ti.n0 : ti.n0;
+      }
+    } else {
+      seglen = C::BNL;
+      seg0 = ti.n0 + rank * C::BNL;
+    }
     bool ok = true;
     for (int kb = 0; kb < ti.nk; ++kb, ++it) {
       const int s = it % C::STAGES;
       const uint32_t par = ((it / C::STAGES) & 1) ^ 1;
-      if (!wait_bar(&empty[s], par, wc)) { ok = false; break; }
+      if (!wait_bar_p<C>(&empty[s], par, wc)) { ok = false; break; }
       uint8_t* sA = stages + s * C::STAGE_BYTES;
       uint8_t* sB = sA + C::A_BYTES;
-      mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+      uint32_t fbar = 0;
+      if constexpr (C::PAIR == 2) fbar = mapa_shared(smem_u32(&full[s]), 0);
+      if (rank == 0) mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES * C::PAIR);
       const int k0 = kb * C::BK;
       // A operand: M-major boxes (weight gradients) or one K-major box
       if (g.a_mn) {
 #pragma unroll
         for (int j = 0; j < 128 / C::ATOM; ++j)
-          tma_load_2d(sA + j * C::ATOM_BYTES, &g.tmA, ti.m0 + j * C::ATOM, ti.kbase + k0, &full[s]);
+          tma_load<C>(sA + j * C::ATOM_BYTES, &g.tmA, ti.m0 + j * C::ATOM, ti.kbase + k0, &full[s],
+                      fbar);
       } else {
-        tma_load_2d(sA, &g.tmA, ti.kbase + k0, ti.m0, &full[s]);
+        tma_load<C>(sA, &g.tmA, ti.kbase + k0, ti.m0, &full[s], fbar);
       }
       // B operand
       if (!g.b_mn) {
         const int yrow = ti.kind == GK_DW ? 0 : ti.e * g.b_expert_rows;
-        if (ti.kind == GK_FWD1) {   // gate rows then up rows, BN/2 each
-          tma_load_2d(sB, &g.tmB, ti.kbase + k0, yrow + ti.n0, &full[s]);
-          tma_load_2d(sB + (C::BN / 2) * 128, &g.tmB, ti.kbase + k0, yrow + g.I + ti.n0, &full[s]);
-        } else {
-          tma_load_2d(sB, &g.tmB, ti.kbase + k0, yrow + ti.n0, &full[s]);
-        }
+        tma_load<C>(sB, &g.tmB, ti.kbase + k0, yrow + seg0, &full[s], fbar);
+        if (seg1 >= 0)
+          tma_load<C>(sB + seglen * 128, &g.tmB, ti.kbase + k0, yrow + seg1, &full[s], fbar);
       } else {
         const int yb = ti.kind == GK_DW ? ti.kbase + k0 : ti.e * g.b_expert_rows + k0;
-        constexpr int NA = C::BN / C::ATOM;
-#pragma unroll
-        for (int j = 0; j < NA; ++j) {
-          int x;
-          if (ti.kind == GK_FWD1) {
-            constexpr int HALF = NA / 2 > 0 ? NA / 2 : 1;  // host keeps BN >= 2*ATOM
-            x = (j / HALF) * g.I + ti.n0 + (j % HALF) * C::ATOM;
-          } else {
-            x = ti.n0 + j * C::ATOM;
-          }
-          tma_load_2d(sB + j * C::ATOM_BYTES, &g.tmB, x, yb, &full[s]);
-        }
+        const int na = seglen / C::ATOM;
+        for (int j = 0; j < na; ++j)
+          tma_load<C>(sB + j * C::ATOM_BYTES, &g.tmB, seg0 + j * C::ATOM, yb, &full[s], fbar);
+        if (seg1 >= 0)
+          for (int j = 0; j < na; ++j)
+            tma_load<C>(sB + (na + j) * C::ATOM_BYTES, &g.tmB, seg1 + j * C::ATOM, yb, &full[s],
+                        fbar);
       }
     }
     if (!ok) break;
   }
-  // Drain: the latest use of every stage must have landed before exit.
-  const int n = it < C::STAGES ? it : C::STAGES;
-  for (int q = 1; q <= n; ++q) {
-    const int u = it - q;
-    wait_bar_drain(&full[u % C::STAGES], (u / C::STAGES) & 1, wc.limit_ns);
+  // Drain: the latest use of every stage must have landed before exit (the
+  // leader owns the full barriers, which also count the peer's bytes).
+  if (rank == 0) {
+    const int n = it < C::STAGES ? it : C::STAGES;
+    for (int q = 1; q <= n; ++q) {
+      const int u = it - q;
+      wait_bar_drain(&full[u % C::STAGES], (u / C::STAGES) & 1, wc.limit_ns);
+    }
   }
 }
 
+// MMA issuer: one thread of the (leader) CTA.
 template <class C>
 __device__ void mma_role(const EngineParams& P, const int* cum, int total, const int* s_po,
-                         uint8_t* stages, uint64_t* full, uint64_t* empty, uint64_t* tfull,
-                         uint64_t* tempty, uint64_t* drain, uint32_t tmem_base,
+                         const int* s_pt, uint8_t* stages, uint64_t* full, uint64_t* empty,
+                         uint64_t* tfull, uint64_t* tempty, uint64_t* drain, uint32_t tmem_base,
                          const WaitCtl& wc) {
   int it = 0, acc = 0;
   const uint32_t sbase = smem_u32(stages);
-  for (int t = blockIdx.x; t < total; t += gridDim.x) {
-    const Tile ti = decode_tile<C>(P, cum, s_po, t);
+  const int cl = blockIdx.x / C::PAIR, ncl = gridDim.x / C::PAIR;
+  for (int t = cl; t < total; t += ncl) {
+    const Tile ti = decode_tile<C>(P, cum, s_po, s_pt, t, 0);
     const int buf = acc & 1;
-    if (!wait_bar(&tempty[buf], ((acc >> 1) & 1) ^ 1, wc)) break;
+    if (!wait_bar_p<C>(&tempty[buf], ((acc >> 1) & 1) ^ 1, wc)) break;
     tc_fence_after();
     const uint32_t d = tmem_base + buf * C::BN;
-    if (ti.nk == 0) {
-      mbar_arrive(&tfull[buf]);
+    if (ti.nk == 0) {                       // empty expert: nothing to accumulate
+      if constexpr (C::PAIR == 2) tc_commit_pair(&tfull[buf], 3); else mbar_arrive(&tfull[buf]);
       ++acc;
       continue;
     }
@@ -277,11 +349,11 @@ __device__ void mma_role(const EngineParams& P, const int* cum, int total, const
     const uint32_t b_mn = g.b_mn ? 1u : 0u;
     const uint32_t idesc = (1u << 4) | (C::FMT << 7) | (C::FMT << 10) | (a_mn << 15) |
                            (b_mn << 16) | ((uint32_t)(C::BN >> 3) << 17) |
-                           ((uint32_t)(128 >> 4) << 24);
+                           ((uint32_t)((128 * C::PAIR) >> 4) << 24);
     bool ok = true;
     for (int kb = 0; kb < ti.nk; ++kb, ++it) {
       const int s = it % C::STAGES;
-      if (!wait_bar(&full[s], (it / C::STAGES) & 1, wc)) { ok = false; break; }
+      if (!wait_bar_p<C>(&full[s], (it / C::STAGES) & 1, wc)) { ok = false; break; }
       tc_fence_after();
       const uint32_t aA = sbase + s * C::STAGE_BYTES;
       const uint32_t aB = aA + C::A_BYTES;
@@ -291,19 +363,21 @@ __device__ void mma_role(const EngineParams& P, const int* cum, int total, const
                                  : smem_desc_sw128(aA + kk * 32, 16, 1024);
         const uint64_t bd = b_mn ? smem_desc_sw128(aB + kk * C::MN_KSTEP_BYTES, C::ATOM_BYTES, 1024)
                                  : smem_desc_sw128(aB + kk * 32, 16, 1024);
-        if constexpr (C::ES == 2)
+        if constexpr (C::PAIR == 2)
+          mma_f16_pair(d, ad, bd, idesc, (kb | kk) != 0);
+        else if constexpr (C::ES == 2)
           mma_f16(d, ad, bd, idesc, (kb | kk) != 0);
         else
           mma_tf32(d, ad, bd, idesc, (kb | kk) != 0);
       }
-      tc_commit(&empty[s]);
+      if constexpr (C::PAIR == 2) tc_commit_pair(&empty[s], 3); else tc_commit(&empty[s]);
     }
     if (!ok) break;
-    tc_commit(&tfull[buf]);
+    if constexpr (C::PAIR == 2) tc_commit_pair(&tfull[buf], 3); else tc_commit(&tfull[buf]);
     ++acc;
   }
   // Drain every MMA issued by this thread before TMEM is released.
-  tc_commit(drain);
+  if constexpr (C::PAIR == 2) tc_commit_pair(drain, 1); else tc_commit(drain);
   wait_bar_drain(drain, 0, wc.limit_ns);
 }
 
@@ -350,27 +424,33 @@ __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: 
 
 template <class C, typename Elt>
 __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, const int* s_po,
-                              uint64_t* tfull, uint64_t* tempty, uint32_t tmem_base,
-                              volatile int* s_go, const WaitCtl& wc) {
+                              const int* s_pt, int rank, uint64_t* tfull, uint64_t* tempty,
+                              uint32_t tmem_base, volatile int* s_go, const WaitCtl& wc) {
   const int q = (threadIdx.x >> 5) & 3;      // TMEM lane quarter of this warp
   const int lane = threadIdx.x & 31;
   const int r = q * 32 + lane;               // tile row of this thread
   const bool leader = threadIdx.x == 64;     // first epilogue thread
+  const int cl = blockIdx.x / C::PAIR, ncl = gridDim.x / C::PAIR;
+  // the accumulator is released on the MMA-issuing CTA's barrier
+  const uint32_t tempty_cl0 = C::PAIR == 2 ? mapa_shared(smem_u32(&tempty[0]), 0) : 0;
+  const uint32_t tempty_cl1 = C::PAIR == 2 ? mapa_shared(smem_u32(&tempty[1]), 0) : 0;
   int acc = 0;
-  for (int t = blockIdx.x; t < total; t += gridDim.x) {
-    const Tile ti = decode_tile<C>(P, cum, s_po, t);
+  for (int t = cl; t < total; t += ncl) {
+    const Tile ti = decode_tile<C>(P, cum, s_po, s_pt, t, rank);
     const GemmProblem& g = P.prob[ti.p];
     const int buf = acc & 1;
     // One thread waits; the decision is shared so all 128 threads take the
     // same path through the named barriers below.
-    if (leader) s_go[buf] = wait_bar(&tfull[buf], (acc >> 1) & 1, wc) ? 1 : 0;
+    if (leader) s_go[buf] = wait_bar_p<C>(&tfull[buf], (acc >> 1) & 1, wc) ? 1 : 0;
     epi_bar();
     if (!s_go[buf]) break;
     tc_fence_after();
     __syncwarp();
     const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * C::BN;
     float v[32], w[32];
-    if (ti.kind == GK_FWD1) {
+    if (!ti.valid) {
+      // rows past the tile's expert (odd m-block count) or past M: no output
+    } else if (ti.kind == GK_FWD1) {
       const int row = ti.m0 + r;
       Elt* outA = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
       Elt* h13 = g.out2 ? static_cast<Elt*>(g.out2) + (size_t)row * g.ld_out2 + ti.n0 : nullptr;
@@ -388,7 +468,11 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       }
     } else if (ti.kind == GK_FWD2) {
       const int row = ti.m0 + r;
-      const int a = g.assign_of_row[row];
+      int a = g.assign_of_row[row];
+      if (a >= g.n_assign) {          // corrupted map: treat as a pad row
+        report(P.status, MOE_ERR_BAD_INDEX);
+        a = -1;
+      }
       const float gt = a >= 0 ? g.gate[a] : 0.f;
       Elt* out = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
 #pragma unroll 1
@@ -400,7 +484,11 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       }
     } else if (ti.kind == GK_BWD_D) {
       const int row = ti.m0 + r;
-      const int a = g.assign_of_row[row];
+      int a = g.assign_of_row[row];
+      if (a >= g.n_assign) {          // corrupted map: treat as a pad row
+        report(P.status, MOE_ERR_BAD_INDEX);
+        a = -1;
+      }
       const float gt = a >= 0 ? g.gate[a] : 0.f;
       const Elt* h13 = static_cast<const Elt*>(g.aux) + (size_t)row * g.ld_aux + ti.n0;
       Elt* dh = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
@@ -448,8 +536,12 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       }
     }
     tc_fence_before();
-    mbar_arrive(&tempty[buf]);
-    if (g.signal) {
+    __syncwarp();
+    if (lane == 0) {
+      if constexpr (C::PAIR == 2) mbar_arrive_cluster(buf ? tempty_cl1 : tempty_cl0);
+      else mbar_arrive(&tempty[buf]);
+    }
+    if (g.signal && ti.valid) {
       // Publish this tile's rows to TMA readers in other CTAs.
       fence_proxy_async_global();
       __threadfence();
@@ -461,9 +553,9 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
 }
 
 // ----------------------------------------------------------------- kernel
-template <typename Elt, int BN>
+template <typename Elt, int BN, int PAIR>
 __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant__ EngineParams P) {
-  using C = Cfg<Elt, BN>;
+  using C = Cfg<Elt, BN, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* stages = smem;
@@ -477,8 +569,10 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
   int* s_go = abort_flag + 1;           // [2]
   int* s_po = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + 256);
+  int* s_pt = s_po + (kMaxE + 1);       // pair tiles before expert e (PAIR == 2)
 
   const int warp = threadIdx.x >> 5;
+  const int rank = PAIR == 2 ? (int)cluster_ctarank() : 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -486,7 +580,7 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 128);
+      mbar_init(&tempty[b], 4 * PAIR);  // one arrival per epilogue warp of the pair
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -494,15 +588,40 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
     fence_barrier_init();
   }
   for (int i = threadIdx.x; i <= P.E; i += blockDim.x) s_po[i] = P.padded_offsets[i];
-  if (warp == 1) tmem_alloc(tmem_holder, C::TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (PAIR == 2) tmem_alloc_pair(tmem_holder, C::TMEM_COLS);
+    else tmem_alloc(tmem_holder, C::TMEM_COLS);
+  }
   if (threadIdx.x == 0) {
     for (int p = 0; p < P.nprob; ++p) {
       tma_prefetch_desc(&P.prob[p].tmA);
       tma_prefetch_desc(&P.prob[p].tmB);
     }
   }
+  __syncthreads();
+  if constexpr (PAIR == 2) {
+    // exclusive scan of ceil(m-blocks / 2) over experts (warp 2)
+    if (warp == 2) {
+      const int lane = threadIdx.x & 31;
+      int carry = 0;
+      for (int c0 = 0; c0 < P.E; c0 += 32) {
+        const int e = c0 + lane;
+        const int v = e < P.E ? ((s_po[e + 1] - s_po[e]) / 128 + 1) / 2 : 0;
+        int x = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, off);
+          if (lane >= off) x += y;
+        }
+        if (e < P.E) s_pt[e] = carry + x - v;
+        carry += __shfl_sync(0xffffffffu, x, 31);
+      }
+      if (lane == 0) s_pt[P.E] = carry;
+    }
+  }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR == 2) cluster_sync_all();   // peers' barriers exist before use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
@@ -514,7 +633,10 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
     int n = 0;
     if (p < P.nprob) {
       const GemmProblem& g = P.prob[p];
-      n = g.kind == GK_DW ? P.E * ((g.M + 127) / 128) * g.nt : (tpad / 128) * g.nt;
+      if (g.kind == GK_DW)
+        n = P.E * (((g.M + 127) / 128 + PAIR - 1) / PAIR) * g.nt;
+      else
+        n = (PAIR == 2 ? s_pt[P.E] : tpad / 128) * g.nt;
     }
     cum[p + 1] = cum[p] + n;
   }
@@ -522,19 +644,35 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
   const WaitCtl wc{abort_flag, P.status, P.wait_ns};
 
   if (warp == 0) {
-    if ((threadIdx.x & 31) == 0) producer_role<C>(P, cum, total, s_po, stages, full, empty, wc);
+    if ((threadIdx.x & 31) == 0)
+      producer_role<C>(P, cum, total, s_po, s_pt, rank, stages, full, empty, wc);
     __syncwarp();
   } else if (warp == 1) {
-    if ((threadIdx.x & 31) == 0)
-      mma_role<C>(P, cum, total, s_po, stages, full, empty, tfull, tempty, drain, tmem_base, wc);
+    if ((threadIdx.x & 31) == 0 && rank == 0)
+      mma_role<C>(P, cum, total, s_po, s_pt, stages, full, empty, tfull, tempty, drain, tmem_base,
+                  wc);
     __syncwarp();
   } else {
-    epilogue_role<C, Elt>(P, cum, total, s_po, tfull, tempty, tmem_base, s_go, wc);
+    epilogue_role<C, Elt>(P, cum, total, s_po, s_pt, rank, tfull, tempty, tmem_base, s_go, wc);
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR == 2) {
+    // After an abort, copies issued by either CTA of the pair may still be
+    // in flight towards the other; give them time to land before the pair
+    // leaves (they complete in microseconds).
+    if (threadIdx.x == 0 && *abort_flag) {
+      const uint64_t t0 = global_ns();
+      while (global_ns() - t0 < 200000) __nanosleep(1000);
+    }
+    __syncthreads();
+    cluster_sync_all();
+  }
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (PAIR == 2) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
 }
 
 // ------------------------------------------------------------------- host
@@ -581,22 +719,51 @@ int sm_count() {
   return sms[dev] > 0 ? sms[dev] : 1;
 }
 
-template <typename Elt, int BN>
+template <typename Elt, int BN, int PAIR>
 cudaError_t launch_typed(const EngineParams& P, int64_t tile_bound, cudaStream_t s) {
-  using C = Cfg<Elt, BN>;
+  using C = Cfg<Elt, BN, PAIR>;
+  auto kern = moe_gemm_kernel<Elt, BN, PAIR>;
   static bool attr_set[64] = {false};
+  static int max_clusters[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<Elt, BN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  int grid = sm_count();
-  if (tile_bound < grid) grid = (int)(tile_bound < 1 ? 1 : tile_bound);
-  moe_gemm_kernel<Elt, BN><<<grid, 192, C::SMEM_BYTES, s>>>(P);
-  return cudaGetLastError();
+  if constexpr (PAIR == 1) {
+    int grid = sm_count();
+    if (tile_bound < grid) grid = (int)(tile_bound < 1 ? 1 : tile_bound);
+    kern<<<grid, 192, C::SMEM_BYTES, s>>>(P);
+    return cudaGetLastError();
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(192, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (!max_clusters[dev]) {
+      // every cluster must be resident at once (tiles wait on other tiles)
+      cfg.gridDim = dim3(2 * (sm_count() / 2), 1, 1);
+      int n = 0;
+      cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess || n < 1) return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
+      max_clusters[dev] = n;
+    }
+    int64_t clusters = max_clusters[dev];
+    if (tile_bound < clusters) clusters = tile_bound < 1 ? 1 : tile_bound;
+    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+    return cudaLaunchKernelEx(&cfg, kern, P);
+  }
 }
 
 }  // namespace
@@ -614,6 +781,9 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
   P.wait_ns = L.wait_ns;
   const int es = L.elem_bytes;
   const int BK = 128 / es, ATOM = 128 / es;
+  // bf16 runs 256-row tiles over an SM pair (B split in halves of >= 64
+  // columns); TF32 and narrow tiles run on single CTAs.
+  const int pair = es == 2 && L.BN >= 128 && !(debug_flags() & MOE_DEBUG_SINGLE_CTA) ? 2 : 1;
   int64_t tile_bound = 0;
   const int64_t mblocks_max = (L.max_rows + 127) / 128;
   for (int p = 0; p < L.nprob; ++p) {
@@ -637,6 +807,7 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
     g.aux = d.aux;
     g.gate = d.gate;
     g.assign_of_row = d.assign_of_row;
+    g.n_assign = d.n_assign;
     g.partial = d.partial;
     const bool a_mn = d.a_mn != 0;
     const bool b_mn = d.b_mn != 0;
@@ -650,21 +821,26 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
                    : make_tmap(&g.tmA, d.a, es, d.a_rows, d.a_cols, BK, 128);
     ok = ok && (b_mn ? make_tmap(&g.tmB, d.b, es, d.b_rows, d.b_cols, ATOM, BK)
                      : make_tmap(&g.tmB, d.b, es, d.b_rows, d.b_cols, BK,
-                                 d.kind == GK_FWD1 ? L.BN / 2 : L.BN));
+                                 d.kind == GK_FWD1 ? L.BN / 2 : L.BN / pair));
     if (!ok) { *st = MOE_ERR_CUDA; return cudaSuccess; }
     tile_bound += d.kind == GK_DW ? (int64_t)L.E * ((d.M + 127) / 128) * g.nt : mblocks_max * g.nt;
   }
-  if (es == 2) {
+  if (es == 2 && pair == 2) {
     switch (L.BN) {
-      case 256: return launch_typed<__nv_bfloat16, 256>(P, tile_bound, s);
-      case 128: return launch_typed<__nv_bfloat16, 128>(P, tile_bound, s);
-      case 64: return launch_typed<__nv_bfloat16, 64>(P, tile_bound, s);
+      case 256: return launch_typed<__nv_bfloat16, 256, 2>(P, tile_bound, s);
+      case 128: return launch_typed<__nv_bfloat16, 128, 2>(P, tile_bound, s);
+    }
+  } else if (es == 2) {
+    switch (L.BN) {
+      case 256: return launch_typed<__nv_bfloat16, 256, 1>(P, tile_bound, s);
+      case 128: return launch_typed<__nv_bfloat16, 128, 1>(P, tile_bound, s);
+      case 64: return launch_typed<__nv_bfloat16, 64, 1>(P, tile_bound, s);
     }
   } else if (es == 4) {
     switch (L.BN) {
-      case 256: return launch_typed<float, 256>(P, tile_bound, s);
-      case 128: return launch_typed<float, 128>(P, tile_bound, s);
-      case 64: return launch_typed<float, 64>(P, tile_bound, s);
+      case 256: return launch_typed<float, 256, 1>(P, tile_bound, s);
+      case 128: return launch_typed<float, 128, 1>(P, tile_bound, s);
+      case 64: return launch_typed<float, 64, 1>(P, tile_bound, s);
     }
   }
   *st = MOE_ERR_UNSUPPORTED;

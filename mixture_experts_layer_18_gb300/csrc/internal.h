@@ -70,6 +70,7 @@ struct GemmDesc {
   int ld_aux;
   const float* gate;
   const int32_t* assign_of_row;
+  int n_assign;
   float* partial;
 };
 

@@ -318,7 +318,7 @@ moe_status moe_forward(const moe_dims* d, const void* X, const void* W13, const 
     }
     g.N = d->H; g.K = d->I;
     g.out = zg; g.ld_out = d->H;
-    g.gate = r->gate; g.assign_of_row = r->assign_of_row;
+    g.gate = r->gate; g.assign_of_row = r->assign_of_row; g.n_assign = n_assign;
     MOE_TRY(launch_engine(L, s, &st));
     if (st != MOE_OK) return st;
   }
@@ -391,7 +391,7 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
   gd.N = d->I; gd.K = d->H; gd.b_expert_rows = d->I; gd.I = d->I;
   gd.out = dh13; gd.ld_out = 2 * d->I;
   gd.aux = h13; gd.ld_aux = 2 * d->I;
-  gd.gate = r->gate; gd.assign_of_row = r->assign_of_row;
+  gd.gate = r->gate; gd.assign_of_row = r->assign_of_row; gd.n_assign = n_assign;
   gd.partial = partial;
   // dW2_e = A_e^T (gate * dY)_perm_e   (needs nothing from this launch)
   GemmDesc gw2{};

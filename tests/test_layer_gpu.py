@@ -82,6 +82,18 @@ def test_small_shapes_full(name):
     _check_small(SMALL[name])
 
 
+@pytest.mark.parametrize("name", ["bf16_a", "bf16_odd_I", "bf16_k1"])
+def test_small_shapes_single_cta_tiles(name):
+    """The bf16 engine with single-CTA 128-row tiles (instead of 256-row tiles
+    over an SM pair) gives the same parity."""
+    import mixture_experts_layer_18_gb300 as M
+    M.moe_set_debug(M.MOE_DEBUG_SINGLE_CTA, 0)
+    try:
+        _check_small(SMALL[name])
+    finally:
+        M.moe_set_debug(0, 0)
+
+
 def test_skewed_routing_with_empty_experts():
     cfg = MoEConfig("skew_small", 600, 256, 32, 4, 128, "bf16", skew=True)
     inp = make_inputs(cfg)
