@@ -72,6 +72,10 @@ struct GemmProblem {
   const int32_t* assign_of_row;
   int n_assign;      // valid assignment indices are [0, n_assign)
   float* partial;
+  // MXFP8 operands: E8M0 scale atoms (512 B per 128 MN indices x 128 K)
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  int sfa_kg, sfb_kg;  // K groups of 128 in each operand's 2-D view
 };
 
 struct EngineParams {
@@ -87,6 +91,7 @@ struct EngineParams {
 
 template <typename Elt, int BN_, int PAIR_>
 struct Cfg {
+  static constexpr bool MX = sizeof(Elt) == 1;    // MXFP8 (E4M3 + E8M0 block scales)
   static constexpr int PAIR = PAIR_;              // CTAs per MMA tile (1, or 2 = SM pair)
   static constexpr int BN = BN_;                  // MMA N = accumulator columns
   static constexpr int BNL = BN / PAIR;           // B columns staged by each CTA
@@ -96,13 +101,19 @@ struct Cfg {
   static constexpr int A_BYTES = 128 * 128;       // 128 rows x 128 bytes
   static constexpr int B_BYTES = BNL * 128;
   static constexpr int ATOM_BYTES = BK * 128;     // one MN-major column block
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES_RAW = 196608 / STAGE_BYTES;
+  static constexpr int SFA_BYTES = MX ? 512 : 0;              // one scale atom for A
+  static constexpr int SFB_BYTES = MX ? (BNL / 128) * 512 : 0; // B atoms (BNL % 128 == 0)
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int STAGES_RAW = (MX ? 204800 : 196608) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-  static constexpr int TMEM_COLS = 2 * BN;
+  // TMEM: NACC accumulators of BN columns; MXFP8 keeps one accumulator and a
+  // 16-column scale slot per pipeline stage from column 256 on.
+  static constexpr int NACC = MX ? 1 : 2;
+  static constexpr int SF_COL0 = 256;
+  static constexpr int TMEM_COLS = MX ? 512 : 2 * BN;
   static constexpr int KSTEPS = 4;                // MMAs per stage (32 bytes of K each)
   static constexpr int MN_KSTEP_BYTES = (32 / ES) * 128;  // MN-major advance per MMA
-  static constexpr uint32_t FMT = ES == 2 ? 1u : 2u;      // BF16 : TF32
+  static constexpr uint32_t FMT = ES == 2 ? 1u : (ES == 4 ? 2u : 0u);  // BF16 : TF32 : E4M3
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*bars*/ +
                                     2 * (kMaxE + 1) * 4 + 64;
 };
@@ -295,13 +306,13 @@ __device__ void producer_role(const EngineParams& P, const int* cum, int total, 
         tma_load<C>(sA, &g.tmA, ti.kbase + k0, ti.m0, &full[s], fbar);
       }
       // B operand
+      const int yrow = ti.kind == GK_DW ? 0 : ti.e * g.b_expert_rows;
+      const int yb = ti.kind == GK_DW ? ti.kbase + k0 : ti.e * g.b_expert_rows + k0;
       if (!g.b_mn) {
-        const int yrow = ti.kind == GK_DW ? 0 : ti.e * g.b_expert_rows;
         tma_load<C>(sB, &g.tmB, ti.kbase + k0, yrow + seg0, &full[s], fbar);
         if (seg1 >= 0)
           tma_load<C>(sB + seglen * 128, &g.tmB, ti.kbase + k0, yrow + seg1, &full[s], fbar);
       } else {
-        const int yb = ti.kind == GK_DW ? ti.kbase + k0 : ti.e * g.b_expert_rows + k0;
         const int na = seglen / C::ATOM;
         for (int j = 0; j < na; ++j)
           tma_load<C>(sB + j * C::ATOM_BYTES, &g.tmB, seg0 + j * C::ATOM, yb, &full[s], fbar);
@@ -309,6 +320,25 @@ __device__ void producer_role(const EngineParams& P, const int* cum, int total, 
           for (int j = 0; j < na; ++j)
             tma_load<C>(sB + (na + j) * C::ATOM_BYTES, &g.tmB, seg1 + j * C::ATOM, yb, &full[s],
                         fbar);
+      }
+      if constexpr (C::MX) {
+        // scale atoms: A's 128 rows x this K block, then B's column blocks
+        uint8_t* sSFA = sB + C::B_BYTES;
+        uint8_t* sSFB = sSFA + C::SFA_BYTES;
+        bulk_load(sSFA,
+                  g.sfa + ((size_t)(ti.m0 >> 7) * g.sfa_kg + ((ti.kbase + k0) >> 7)) * 512, 512,
+                  &full[s]);
+        const int kidx = g.b_mn ? yb : ti.kbase + k0;
+        int ai = 0;
+        for (int sg = 0; sg < 2; ++sg) {
+          const int seg = sg ? seg1 : seg0;
+          if (seg < 0) continue;
+          for (int j = 0; j < seglen / 128; ++j, ++ai) {
+            const int mn = (g.b_mn ? 0 : yrow) + seg + 128 * j;
+            bulk_load(sSFB + ai * 512,
+                      g.sfb + ((size_t)(mn >> 7) * g.sfb_kg + (kidx >> 7)) * 512, 512, &full[s]);
+          }
+        }
       }
     }
     if (!ok) break;
@@ -335,8 +365,8 @@ __device__ void mma_role(const EngineParams& P, const int* cum, int total, const
   const int cl = blockIdx.x / C::PAIR, ncl = gridDim.x / C::PAIR;
   for (int t = cl; t < total; t += ncl) {
     const Tile ti = decode_tile<C>(P, cum, s_po, s_pt, t, 0);
-    const int buf = acc & 1;
-    if (!wait_bar_p<C>(&tempty[buf], ((acc >> 1) & 1) ^ 1, wc)) break;
+    const int buf = acc % C::NACC;
+    if (!wait_bar_p<C>(&tempty[buf], ((acc / C::NACC) & 1) ^ 1, wc)) break;
     tc_fence_after();
     const uint32_t d = tmem_base + buf * C::BN;
     if (ti.nk == 0) {                       // empty expert: nothing to accumulate
@@ -347,8 +377,11 @@ __device__ void mma_role(const EngineParams& P, const int* cum, int total, const
     const GemmProblem& g = P.prob[ti.p];
     const uint32_t a_mn = g.a_mn ? 1u : 0u;
     const uint32_t b_mn = g.b_mn ? 1u : 0u;
-    const uint32_t idesc = (1u << 4) | (C::FMT << 7) | (C::FMT << 10) | (a_mn << 15) |
-                           (b_mn << 16) | ((uint32_t)(C::BN >> 3) << 17) |
+    // instruction descriptor: D fp32 (dense kinds), operand formats, majors,
+    // N >> 3, M >> 4; the MXFP8 kind instead carries E8M0 scales (bit 23)
+    // and the scale byte of each MMA (bits 4-5 for B, 29-30 for A).
+    const uint32_t idesc = (C::MX ? (1u << 23) : (1u << 4)) | (C::FMT << 7) | (C::FMT << 10) |
+                           (a_mn << 15) | (b_mn << 16) | ((uint32_t)(C::BN >> 3) << 17) |
                            ((uint32_t)((128 * C::PAIR) >> 4) << 24);
     bool ok = true;
     for (int kb = 0; kb < ti.nk; ++kb, ++it) {
@@ -357,13 +390,26 @@ __device__ void mma_role(const EngineParams& P, const int* cum, int total, const
       tc_fence_after();
       const uint32_t aA = sbase + s * C::STAGE_BYTES;
       const uint32_t aB = aA + C::A_BYTES;
+      uint32_t sf_slot = 0;
+      if constexpr (C::MX) {
+        // scales of this stage into its TMEM slot: A at +0..3, B at +4..
+        sf_slot = tmem_base + C::SF_COL0 + s * 16;
+        const uint32_t aS = aB + C::B_BYTES;
+        tmem_cp_32x128b_x4(sf_slot, smem_desc_rows16(aS));
+#pragma unroll
+        for (int j = 0; j < C::SFB_BYTES / 512; ++j)
+          tmem_cp_32x128b_x4(sf_slot + 4 + 4 * j, smem_desc_rows16(aS + 512 + 512 * j));
+      }
 #pragma unroll
       for (int kk = 0; kk < C::KSTEPS; ++kk) {
         const uint64_t ad = a_mn ? smem_desc_sw128(aA + kk * C::MN_KSTEP_BYTES, C::ATOM_BYTES, 1024)
                                  : smem_desc_sw128(aA + kk * 32, 16, 1024);
         const uint64_t bd = b_mn ? smem_desc_sw128(aB + kk * C::MN_KSTEP_BYTES, C::ATOM_BYTES, 1024)
                                  : smem_desc_sw128(aB + kk * 32, 16, 1024);
-        if constexpr (C::PAIR == 2)
+        if constexpr (C::MX)
+          mma_mxf8(d, ad, bd, idesc | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), sf_slot,
+                   sf_slot + 4, (kb | kk) != 0);
+        else if constexpr (C::PAIR == 2)
           mma_f16_pair(d, ad, bd, idesc, (kb | kk) != 0);
         else if constexpr (C::ES == 2)
           mma_f16(d, ad, bd, idesc, (kb | kk) != 0);
@@ -438,12 +484,13 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
   for (int t = cl; t < total; t += ncl) {
     const Tile ti = decode_tile<C>(P, cum, s_po, s_pt, t, rank);
     const GemmProblem& g = P.prob[ti.p];
-    const int buf = acc & 1;
+    const int buf = acc % C::NACC;
     // One thread waits; the decision is shared so all 128 threads take the
-    // same path through the named barriers below.
-    if (leader) s_go[buf] = wait_bar_p<C>(&tfull[buf], (acc >> 1) & 1, wc) ? 1 : 0;
+    // same path through the named barriers below.  (s_go is indexed by
+    // acc & 1 so a slow reader never sees the next tile's decision.)
+    if (leader) s_go[acc & 1] = wait_bar_p<C>(&tfull[buf], (acc / C::NACC) & 1, wc) ? 1 : 0;
     epi_bar();
-    if (!s_go[buf]) break;
+    if (!s_go[acc & 1]) break;
     tc_fence_after();
     __syncwarp();
     const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * C::BN;
@@ -553,9 +600,9 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
 }
 
 // ----------------------------------------------------------------- kernel
-template <typename Elt, int BN, int PAIR>
+template <typename In, typename Out, int BN, int PAIR>
 __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant__ EngineParams P) {
-  using C = Cfg<Elt, BN, PAIR>;
+  using C = Cfg<In, BN, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* stages = smem;
@@ -653,7 +700,7 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
                   wc);
     __syncwarp();
   } else {
-    epilogue_role<C, Elt>(P, cum, total, s_po, s_pt, rank, tfull, tempty, tmem_base, s_go, wc);
+    epilogue_role<C, Out>(P, cum, total, s_po, s_pt, rank, tfull, tempty, tmem_base, s_go, wc);
   }
   tc_fence_before();
   __syncthreads();
@@ -719,10 +766,10 @@ int sm_count() {
   return sms[dev] > 0 ? sms[dev] : 1;
 }
 
-template <typename Elt, int BN, int PAIR>
+template <typename In, typename Out, int BN, int PAIR>
 cudaError_t launch_typed(const EngineParams& P, int64_t tile_bound, cudaStream_t s) {
-  using C = Cfg<Elt, BN, PAIR>;
-  auto kern = moe_gemm_kernel<Elt, BN, PAIR>;
+  using C = Cfg<In, BN, PAIR>;
+  auto kern = moe_gemm_kernel<In, Out, BN, PAIR>;
   static bool attr_set[64] = {false};
   static int max_clusters[64] = {0};
   int dev = 0;
@@ -809,6 +856,11 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
     g.assign_of_row = d.assign_of_row;
     g.n_assign = d.n_assign;
     g.partial = d.partial;
+    g.sfa = d.sfa;
+    g.sfb = d.sfb;
+    g.sfa_kg = d.sfa_kg;
+    g.sfb_kg = d.sfb_kg;
+    if (es == 1 && (!d.sfa || !d.sfb)) { *st = MOE_ERR_INVALID_ARG; return cudaSuccess; }
     const bool a_mn = d.a_mn != 0;
     const bool b_mn = d.b_mn != 0;
     if ((a_mn || b_mn) && es == 4) { *st = MOE_ERR_UNSUPPORTED; return cudaSuccess; }  // TF32: K-major only
@@ -827,20 +879,22 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
   }
   if (es == 2 && pair == 2) {
     switch (L.BN) {
-      case 256: return launch_typed<__nv_bfloat16, 256, 2>(P, tile_bound, s);
-      case 128: return launch_typed<__nv_bfloat16, 128, 2>(P, tile_bound, s);
+      case 256: return launch_typed<__nv_bfloat16, __nv_bfloat16, 256, 2>(P, tile_bound, s);
+      case 128: return launch_typed<__nv_bfloat16, __nv_bfloat16, 128, 2>(P, tile_bound, s);
     }
   } else if (es == 2) {
     switch (L.BN) {
-      case 256: return launch_typed<__nv_bfloat16, 256, 1>(P, tile_bound, s);
-      case 128: return launch_typed<__nv_bfloat16, 128, 1>(P, tile_bound, s);
-      case 64: return launch_typed<__nv_bfloat16, 64, 1>(P, tile_bound, s);
+      case 256: return launch_typed<__nv_bfloat16, __nv_bfloat16, 256, 1>(P, tile_bound, s);
+      case 128: return launch_typed<__nv_bfloat16, __nv_bfloat16, 128, 1>(P, tile_bound, s);
+      case 64: return launch_typed<__nv_bfloat16, __nv_bfloat16, 64, 1>(P, tile_bound, s);
     }
+  } else if (es == 1) {   // MXFP8 operands, bf16 outputs
+    if (L.BN == 256) return launch_typed<uint8_t, __nv_bfloat16, 256, 1>(P, tile_bound, s);
   } else if (es == 4) {
     switch (L.BN) {
-      case 256: return launch_typed<float, 256, 1>(P, tile_bound, s);
-      case 128: return launch_typed<float, 128, 1>(P, tile_bound, s);
-      case 64: return launch_typed<float, 64, 1>(P, tile_bound, s);
+      case 256: return launch_typed<float, float, 256, 1>(P, tile_bound, s);
+      case 128: return launch_typed<float, float, 128, 1>(P, tile_bound, s);
+      case 64: return launch_typed<float, float, 64, 1>(P, tile_bound, s);
     }
   }
   *st = MOE_ERR_UNSUPPORTED;

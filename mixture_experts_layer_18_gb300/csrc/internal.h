@@ -43,11 +43,14 @@ cudaError_t launch_dgate_reduce(const float* partial, int nt, int n_assign,
                                 const int32_t* row_of_assign, int64_t max_rows, float* dgate,
                                 int32_t* status, cudaStream_t s);
 
-// quant.cu  (bf16 source; plain scale layout: [R, C/32] for axis 1,
-// [R/32, C] for axis 0)
+// quant.cu  (bf16 source).  layout 0: plain scales [R, C/32] (axis 1) or
+// [R/32, C] (axis 0).  layout 1: tensor-core scale atoms, 512 bytes per
+// (128 MN indices, 128 K elements); axis 1 = K along columns (MN = rows,
+// C % 128 == 0, rows padded to 128), axis 0 = K along rows (MN = columns,
+// C % 128 == 0, kgroups = ceil(R/128)).
 cudaError_t launch_quantize(const void* src, int R, int C, int ld, int axis,
                             const int32_t* group_offsets, int G, uint8_t* q, uint8_t* scales,
-                            int32_t* status, cudaStream_t s);
+                            int32_t* status, cudaStream_t s, int layout = 0);
 
 // gemm.cu
 struct GemmDesc {
@@ -72,13 +75,16 @@ struct GemmDesc {
   const int32_t* assign_of_row;
   int n_assign;
   float* partial;
+  const uint8_t* sfa;          // MXFP8: scale atoms of A / B (quant.cu layout 1)
+  const uint8_t* sfb;
+  int sfa_kg, sfb_kg;          // K groups of 128 in each operand's 2-D view
 };
 
 struct EngineLaunch {
   GemmDesc prob[4];
   int nprob;
   int E;
-  int elem_bytes;              // 2: bf16 (kind::f16), 4: fp32 (kind::tf32)
+  int elem_bytes;              // 2: bf16 (kind::f16), 4: fp32 (kind::tf32), 1: MXFP8
   int BN;                      // 64, 128 or 256
   const int32_t* padded_offsets;
   int64_t max_rows;

@@ -45,6 +45,9 @@ constexpr int DEP_NONE = 0, DEP_MBLOCK = 1, DEP_EXPERT = 2;
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 int elem_bytes(const moe_dims* d) { return d->mode == MOE_F32 ? 4 : 2; }
+// MXFP8 GEMMs in the forward (mxfp8) / in the backward (mxfp8, fp8_bwd)
+bool mx_fwd(const moe_dims* d) { return d->mode == MOE_MXFP8; }
+bool mx_bwd(const moe_dims* d) { return d->mode == MOE_MXFP8 || d->mode == MOE_FP8_BWD; }
 
 bool dims_ok(const moe_dims* d) {
   if (!d) return false;
@@ -64,6 +67,7 @@ bool aligned16(const void* p) { return p && ((uintptr_t)p & 15) == 0; }
 
 // Tile width of the forward gate/up GEMM: BN/2 columns of each half per tile.
 int bn_fwd1(const moe_dims* d) {
+  if (mx_fwd(d)) return d->I % 256 == 0 && d->H % 256 == 0 ? 256 : 0;
   const int atom = 128 / elem_bytes(d);
   for (int bn : {256, 128, 64})
     if (bn / 2 >= atom && d->I % (bn / 2) == 0) return bn;
@@ -75,6 +79,7 @@ int bn_div(int n) {
   return 0;
 }
 int bn_bwd(const moe_dims* d) {
+  if (mx_bwd(d)) return d->I % 256 == 0 && d->H % 256 == 0 ? 256 : 0;
   for (int bn : {256, 128, 64})
     if (d->I % bn == 0 && d->H % bn == 0) return bn;
   return 0;
@@ -85,8 +90,24 @@ int bn_bwd(const moe_dims* d) {
 // row pitch is the row capacity rounded up to 32.
 int64_t ld_t(const moe_dims* d) { return (max_rows(d) + 31) / 32 * 32; }
 
+// MXFP8: one quantised operand = E4M3 codes + tensor-core scale atoms.
+struct MxBuf {
+  size_t q, sf;
+};
+int64_t rows_pad(const moe_dims* d) { return (max_rows(d) + 127) / 128 * 128; }
+// codes of an [R, C] operand (R padded to 128 for the atoms)
+MxBuf mx_carve(size_t& o, size_t R, size_t Rp, size_t C) {
+  MxBuf b;
+  b.q = o;
+  o += align256(R * C);
+  b.sf = o;
+  o += align256(Rp * C / 32);
+  return b;
+}
+
 struct FwdWs {
   size_t zg, w13t, w2t, total;
+  MxBuf x, w13, a, w2;     // MXFP8 forward operands
 };
 FwdWs fwd_ws(const moe_dims* d) {
   FwdWs w;
@@ -97,6 +118,13 @@ FwdWs fwd_ws(const moe_dims* d) {
   const bool t = d->mode == MOE_F32;
   w.w13t = o; o += t ? align256(2 * wsz) : 0;
   w.w2t = o; o += t ? align256(wsz) : 0;
+  if (mx_fwd(d)) {
+    const size_t rp = (size_t)rows_pad(d), EH = (size_t)d->E * d->H, EI = (size_t)d->E * d->I;
+    w.x = mx_carve(o, rows, rp, d->H);
+    w.w13 = mx_carve(o, EH, EH, 2 * (size_t)d->I);
+    w.a = mx_carve(o, rows, rp, d->I);
+    w.w2 = mx_carve(o, EI, EI, d->H);
+  }
   w.total = o;
   return w;
 }
@@ -105,6 +133,7 @@ struct BwdWs {
   size_t dy_perm, dyg_perm, dh13, dxp, partial, ready;
   size_t act_t, dyg_t, xp_t, dh13_t, total;
   int nt_d;
+  MxBuf dy, w2r, actc, dygc, dh13r, dh13c, w13r, xpc;   // MXFP8 backward operands
 };
 BwdWs bwd_ws(const moe_dims* d) {
   BwdWs w;
@@ -124,6 +153,18 @@ BwdWs bwd_ws(const moe_dims* d) {
   w.dyg_t = o; o += t ? align256(lt * d->H) : 0;
   w.xp_t = o; o += t ? align256(lt * d->H) : 0;
   w.dh13_t = o; o += t ? align256(lt * 2 * d->I) : 0;
+  if (mx_bwd(d)) {
+    const size_t rp = (size_t)rows_pad(d), EH = (size_t)d->E * d->H, EI = (size_t)d->E * d->I;
+    const size_t H = d->H, I = d->I;
+    w.dy = mx_carve(o, rows, rp, H);
+    w.w2r = mx_carve(o, EI, EI, H);
+    w.actc = mx_carve(o, rows, rp, I);
+    w.dygc = mx_carve(o, rows, rp, H);
+    w.dh13r = mx_carve(o, rows, rp, 2 * I);
+    w.dh13c = mx_carve(o, rows, rp, 2 * I);
+    w.w13r = mx_carve(o, EH, EH, 2 * I);
+    w.xpc = mx_carve(o, rows, rp, H);
+  }
   w.total = o;
   return w;
 }
@@ -170,6 +211,162 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
     if (_e != cudaSuccess) return MOE_ERR_CUDA;         \
   } while (0)
 
+
+// ---------------------------------------------------------------- MXFP8
+// Every GEMM operand is quantised along that GEMM's contraction axis into
+// E4M3 codes plus scale atoms laid out for the tensor cores (quant.cu,
+// layout 1): token-major activations row-wise (K = columns); weights of the
+// forward and token-axis operands of the weight gradients column-wise
+// (K = rows, blocks restarting at each expert's 128-aligned start).
+struct Mx {
+  const void* q;
+  const uint8_t* sf;
+};
+Mx mx_at(char* base, const MxBuf& b) {
+  return Mx{base + b.q, reinterpret_cast<const uint8_t*>(base + b.sf)};
+}
+
+cudaError_t quant_rows(const void* src, int64_t R, int C, const Mx& m, int32_t* st, cudaStream_t s) {
+  return launch_quantize(src, (int)R, C, C, 1, nullptr, 0, (uint8_t*)m.q, (uint8_t*)m.sf, st, s, 1);
+}
+cudaError_t quant_cols(const void* src, int64_t R, int C, const int32_t* go, int G, const Mx& m,
+                       int32_t* st, cudaStream_t s) {
+  return launch_quantize(src, (int)R, C, C, 0, go, G, (uint8_t*)m.q, (uint8_t*)m.sf, st, s, 1);
+}
+
+moe_status forward_mx(const moe_dims* d, const void* W13, const void* W2, const moe_route_out* r,
+                      void* x_perm, void* h13, void* act, void* zg, char* wsb, const FwdWs& w,
+                      int32_t* dev_status, cudaStream_t s) {
+  const int64_t rows = max_rows(d), rp = rows_pad(d);
+  const int H = d->H, I = d->I, E = d->E;
+  const Mx x = mx_at(wsb, w.x), w13 = mx_at(wsb, w.w13), a = mx_at(wsb, w.a), w2 = mx_at(wsb, w.w2);
+  MOE_TRY(quant_rows(x_perm, rows, H, x, dev_status, s));
+  MOE_TRY(quant_cols(W13, (int64_t)E * H, 2 * I, nullptr, 0, w13, dev_status, s));
+  moe_status st;
+  EngineLaunch L;
+  memset(&L, 0, sizeof(L));
+  L.nprob = 1;
+  L.E = E;
+  L.elem_bytes = 1;
+  L.BN = 256;
+  L.padded_offsets = r->padded_offsets;
+  L.max_rows = rows;
+  L.status = dev_status;
+  L.wait_ns = wait_limit_ns();
+  {
+    GemmDesc& g = L.prob[0];
+    g = GemmDesc{};
+    g.kind = GK_FWD1;
+    g.a = x.q; g.a_rows = rows; g.a_cols = H; g.sfa = x.sf; g.sfa_kg = H / 128;
+    g.b_mn = 1;
+    g.b = w13.q; g.b_rows = (int64_t)E * H; g.b_cols = 2 * I; g.b_expert_rows = H;
+    g.sfb = w13.sf; g.sfb_kg = (int)((int64_t)E * H / 128);
+    g.N = 2 * I; g.K = H; g.I = I;
+    g.out = act; g.ld_out = I;
+    g.out2 = d->save_for_backward ? h13 : nullptr; g.ld_out2 = 2 * I;
+    MOE_TRY(launch_engine(L, s, &st));
+    if (st != MOE_OK) return st;
+  }
+  MOE_TRY(quant_rows(act, rows, I, a, dev_status, s));
+  MOE_TRY(quant_cols(W2, (int64_t)E * I, H, nullptr, 0, w2, dev_status, s));
+  {
+    GemmDesc& g = L.prob[0];
+    g = GemmDesc{};
+    g.kind = GK_FWD2;
+    g.a = a.q; g.a_rows = rows; g.a_cols = I; g.sfa = a.sf; g.sfa_kg = I / 128;
+    g.b_mn = 1;
+    g.b = w2.q; g.b_rows = (int64_t)E * I; g.b_cols = H; g.b_expert_rows = I;
+    g.sfb = w2.sf; g.sfb_kg = (int)((int64_t)E * I / 128);
+    g.N = H; g.K = I;
+    g.out = zg; g.ld_out = H;
+    g.gate = r->gate; g.assign_of_row = r->assign_of_row; g.n_assign = d->T * d->top_k;
+    MOE_TRY(launch_engine(L, s, &st));
+    if (st != MOE_OK) return st;
+  }
+  (void)rp;
+  return MOE_OK;
+}
+
+// Backward with MXFP8 GEMMs (modes mxfp8 and fp8_bwd).  dh13 must be
+// quantised before dX and dW13 can read it, so the gradient GEMMs run as
+// two launches: {D + dSwiGLU, dW2}, then {dX, dW13}.
+moe_status backward_mx(const moe_dims* d, const void* W13, const void* W2,
+                       const moe_route_out* r, const void* x_perm, const void* h13,
+                       const void* act, void* dy_perm, void* dyg_perm, void* dh13, void* dxp,
+                       float* partial, void* dW13, void* dW2, char* wsb, const BwdWs& w,
+                       int32_t* dev_status, cudaStream_t s) {
+  const int64_t rows = max_rows(d), rp = rows_pad(d);
+  const int H = d->H, I = d->I, E = d->E;
+  const int kgt = (int)(rp / 128);   // K groups of the token axis
+  const Mx dy = mx_at(wsb, w.dy), w2r = mx_at(wsb, w.w2r), actc = mx_at(wsb, w.actc),
+           dygc = mx_at(wsb, w.dygc), dh13r = mx_at(wsb, w.dh13r), dh13c = mx_at(wsb, w.dh13c),
+           w13r = mx_at(wsb, w.w13r), xpc = mx_at(wsb, w.xpc);
+  const int32_t* po = r->padded_offsets;
+  MOE_TRY(quant_rows(dy_perm, rows, H, dy, dev_status, s));
+  MOE_TRY(quant_rows(W2, (int64_t)E * I, H, w2r, dev_status, s));
+  MOE_TRY(quant_cols(act, rows, I, po, E, actc, dev_status, s));
+  MOE_TRY(quant_cols(dyg_perm, rows, H, po, E, dygc, dev_status, s));
+  EngineLaunch L;
+  memset(&L, 0, sizeof(L));
+  L.E = E;
+  L.elem_bytes = 1;
+  L.BN = 256;
+  L.padded_offsets = po;
+  L.max_rows = rows;
+  L.status = dev_status;
+  L.wait_ns = wait_limit_ns();
+  moe_status st;
+  {
+    L.nprob = 2;
+    GemmDesc& gd = L.prob[0];
+    gd = GemmDesc{};
+    gd.kind = GK_BWD_D;
+    gd.a = dy.q; gd.a_rows = rows; gd.a_cols = H; gd.sfa = dy.sf; gd.sfa_kg = H / 128;
+    gd.b = w2r.q; gd.b_rows = (int64_t)E * I; gd.b_cols = H; gd.b_expert_rows = I;
+    gd.sfb = w2r.sf; gd.sfb_kg = H / 128;
+    gd.N = I; gd.K = H; gd.I = I;
+    gd.out = dh13; gd.ld_out = 2 * I;
+    gd.aux = h13; gd.ld_aux = 2 * I;
+    gd.gate = r->gate; gd.assign_of_row = r->assign_of_row; gd.n_assign = d->T * d->top_k;
+    gd.partial = partial;
+    GemmDesc& gw2 = L.prob[1];
+    gw2 = GemmDesc{};
+    gw2.kind = GK_DW;
+    gw2.a_mn = gw2.b_mn = 1;
+    gw2.a = actc.q; gw2.a_rows = rows; gw2.a_cols = I; gw2.sfa = actc.sf; gw2.sfa_kg = kgt;
+    gw2.b = dygc.q; gw2.b_rows = rows; gw2.b_cols = H; gw2.sfb = dygc.sf; gw2.sfb_kg = kgt;
+    gw2.M = I; gw2.N = H;
+    gw2.out = dW2; gw2.ld_out = H;
+    MOE_TRY(launch_engine(L, s, &st));
+    if (st != MOE_OK) return st;
+  }
+  MOE_TRY(quant_rows(dh13, rows, 2 * I, dh13r, dev_status, s));
+  MOE_TRY(quant_cols(dh13, rows, 2 * I, po, E, dh13c, dev_status, s));
+  MOE_TRY(quant_rows(W13, (int64_t)E * H, 2 * I, w13r, dev_status, s));
+  MOE_TRY(quant_cols(x_perm, rows, H, po, E, xpc, dev_status, s));
+  {
+    L.nprob = 2;
+    GemmDesc& gx = L.prob[0];
+    gx = GemmDesc{};
+    gx.kind = GK_BWD_DX;
+    gx.a = dh13r.q; gx.a_rows = rows; gx.a_cols = 2 * I; gx.sfa = dh13r.sf; gx.sfa_kg = 2 * I / 128;
+    gx.b = w13r.q; gx.b_rows = (int64_t)E * H; gx.b_cols = 2 * I; gx.b_expert_rows = H;
+    gx.sfb = w13r.sf; gx.sfb_kg = 2 * I / 128;
+    gx.N = H; gx.K = 2 * I;
+    gx.out = dxp; gx.ld_out = H;
+    GemmDesc& gw = L.prob[1];
+    gw = GemmDesc{};
+    gw.kind = GK_DW;
+    gw.a_mn = gw.b_mn = 1;
+    gw.a = xpc.q; gw.a_rows = rows; gw.a_cols = H; gw.sfa = xpc.sf; gw.sfa_kg = kgt;
+    gw.b = dh13c.q; gw.b_rows = rows; gw.b_cols = 2 * I; gw.sfb = dh13c.sf; gw.sfb_kg = kgt;
+    gw.M = H; gw.N = 2 * I;
+    gw.out = dW13; gw.ld_out = 2 * I;
+    MOE_TRY(launch_engine(L, s, &st));
+    if (st != MOE_OK) return st;
+  }
+  return MOE_OK;
+}
 }  // namespace
 }  // namespace moe
 
@@ -242,7 +439,6 @@ moe_status moe_forward(const moe_dims* d, const void* X, const void* W13, const 
       !aligned16(ws) || !aligned16(dev_status))
     return MOE_ERR_INVALID_ARG;
   if (d->T > 0 && (!aligned16(X) || !aligned16(Y))) return MOE_ERR_INVALID_ARG;
-  if (d->mode == MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
   const moe_saved_layout sl = saved_layout(d);
   const FwdWs w = fwd_ws(d);
   if (saved_bytes < sl.total || ws_bytes < w.total) return MOE_ERR_INVALID_ARG;
@@ -258,6 +454,17 @@ moe_status moe_forward(const moe_dims* d, const void* X, const void* W13, const 
   void* act = sv + sl.act;
   void* zg = static_cast<char*>(ws) + w.zg;
 
+  if (mx_fwd(d)) {
+    MOE_TRY(launch_gather_rows(X, x_perm, d->H, es, d->top_k, n_assign, r->assign_of_row,
+                               r->padded_offsets, d->E, rows, dev_status, s));
+    EventScope timing(MOE_WS_FORWARD, s);
+    const moe_status st = forward_mx(d, W13, W2, r, x_perm, h13, act, zg, static_cast<char*>(ws),
+                                     w, dev_status, s);
+    if (st != MOE_OK) return st;
+    timing.finish();
+    MOE_TRY(launch_combine(zg, Y, d->T, d->H, es, d->top_k, r->row_of_assign, rows, dev_status, s));
+    return MOE_OK;
+  }
   const bool f32 = d->mode == MOE_F32;
   const void* w13_src = W13;
   const void* w2_src = W2;
@@ -336,7 +543,6 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
     return MOE_ERR_INVALID_ARG;
   if (d->T > 0 && (!aligned16(dY) || !aligned16(dX) || !aligned16(dgate)))
     return MOE_ERR_INVALID_ARG;
-  if (d->mode == MOE_MXFP8 || d->mode == MOE_FP8_BWD) return MOE_ERR_UNSUPPORTED;
   const moe_saved_layout sl = saved_layout(d);
   const BwdWs w = bwd_ws(d);
   if (saved_bytes < sl.total || ws_bytes < w.total) return MOE_ERR_INVALID_ARG;
@@ -363,6 +569,18 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
                              s));
   MOE_TRY(cudaMemsetAsync(ready, 0, ((rows + 127) / 128) * sizeof(int32_t), s));
 
+  if (mx_bwd(d)) {
+    EventScope timing(MOE_WS_BACKWARD, s);
+    const moe_status st = backward_mx(d, W13, W2, r, x_perm, h13, act, dy_perm, dyg_perm, dh13, dxp,
+                                      partial, dW13, dW2, wb, w, dev_status, s);
+    if (st != MOE_OK) return st;
+    timing.finish();
+    MOE_TRY(launch_combine(dxp, dX, d->T, d->H, es, d->top_k, r->row_of_assign, rows, dev_status,
+                           s));
+    MOE_TRY(launch_dgate_reduce(partial, w.nt_d, n_assign, r->row_of_assign, rows, dgate,
+                                dev_status, s));
+    return MOE_OK;
+  }
   const bool f32 = d->mode == MOE_F32;
   const int64_t lt = ld_t(d);
   float* act_t = reinterpret_cast<float*>(wb + w.act_t);

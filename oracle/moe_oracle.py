@@ -38,6 +38,8 @@ Readings taken where the pages are silent (each also listed in the design doc):
   * Rows of expert e are ordered by ascending assignment index a = t*k + j;
     each expert's row range starts at a multiple of ALIGN (=128) rows, with
     zero pad rows (a storage choice; logical counts stay dropless).
+  * In the MXFP8 modes intermediates are stored in bf16 and quantised right
+    before each GEMM, so codes are decided from bf16 values on both sides.
   * MXFP8 block scale: s = floor(log2(amax)) - 8 clamped to [-127, 127]
     (s = -127 for an all-zero block); elements are x / 2^s rounded to nearest
     even on the E4M3 grid, saturating to +-448.  The contraction axis of every
@@ -269,6 +271,25 @@ def _members(idx, e, tokens=None):
     return a
 
 
+def bf16_round(x):
+    """Value of x as an fp32 number stored in bf16: nearest fp32, then the
+    nearest bf16 (ties to even: add 0x7FFF plus the lowest kept bit to the
+    fp32 bit pattern and drop the low 16 bits).  Finite inputs."""
+    u = np.ascontiguousarray(f64(x).astype(np.float32)).view(np.uint32)
+    r = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) & np.uint32(0xFFFF0000)
+    return r.view(np.float32).astype(np.float64)
+
+
+def _stored(mode, phase):
+    """Storage of intermediates that a quantised GEMM reads.  In the MXFP8
+    phases the layer keeps activations in BF16 and quantises them right
+    before each GEMM ([MM]: BF16 storage, MXFP8 GEMMs), so the E4M3 codes are
+    decided from bf16 values; the oracle takes the same decision from the same
+    precision.  Identity elsewhere (the plain float64 definition)."""
+    use_mx = mode == "mxfp8" or (mode == "fp8_bwd" and phase == "bwd")
+    return bf16_round if use_mx else f64
+
+
 def _gemm_operands(mode, phase):
     """Quantise-dequantise transform applied to GEMM operands: identity for
     f32/bf16, MXFP8 along the contraction axis for mxfp8 (both phases) and
@@ -294,6 +315,7 @@ def forward(X, W13, W2, idx, gate, tokens=None, mode="bf16", keep=False):
     I = I2 // 2
     k = np.asarray(idx).shape[1]
     q = _gemm_operands(mode, "fwd")
+    st = _stored(mode, "fwd")
     tok = np.arange(T) if tokens is None else np.asarray(tokens)
     pos = {int(t): i for i, t in enumerate(tok)}
     Y = np.zeros((len(tok), H))
@@ -308,7 +330,7 @@ def forward(X, W13, W2, idx, gate, tokens=None, mode="bf16", keep=False):
         h = x @ q(W13[e], 0)                             # W13_e blocked along H
         u, v = h[:, :I], h[:, I:]
         A = silu(u) * v
-        z = q(A, 1) @ q(W2[e], 0)                        # blocked along I
+        z = q(st(A), 1) @ q(W2[e], 0)                    # blocked along I
         contrib = g_flat[a][:, None] * z
         for r, tt in enumerate(t):
             Y[pos[int(tt)]] += contrib[r]
@@ -337,7 +359,8 @@ def backward(X, W13, W2, idx, gate, dY, tokens=None, experts=None, mode="bf16"):
     ``experts``).  Either may be None (all).  In mxfp8 / fp8_bwd mode every
     backward GEMM operand is MXFP8-quantised along its contraction axis; the
     token-axis operands of the weight-gradient GEMMs are blocked in 32-row
-    groups of the expert's rows in ascending assignment order, zero padded.
+    groups of the expert's rows in ascending assignment order, zero padded;
+    the stored intermediates (h, A, dh, gate * dY) are bf16 values.
     Returns dict(dX, dgate, dW13, dW2)."""
     X = np.asarray(X)
     T, H = X.shape
@@ -346,6 +369,7 @@ def backward(X, W13, W2, idx, gate, dY, tokens=None, experts=None, mode="bf16"):
     k = np.asarray(idx).shape[1]
     qf = _gemm_operands(mode, "fwd")
     qb = _gemm_operands(mode, "bwd")
+    stb = _stored(mode, "bwd")
     tok = np.arange(T) if tokens is None else np.asarray(tokens)
     exp_list = list(range(E)) if experts is None else [int(e) for e in experts]
     pos = {int(t): i for i, t in enumerate(tok)}
@@ -363,8 +387,11 @@ def backward(X, W13, W2, idx, gate, dY, tokens=None, experts=None, mode="bf16"):
             continue
         t = a // k
         g = g_flat[a][:, None]
-        # forward recomputation (the forward's own precision)
+        # forward recomputation (the forward's own precision); in the MXFP8
+        # backward the saved h and A are the stored (bf16) ones
         h = qf(X[t], 1) @ qf(W13[e], 0)
+        A_saved = stb((h[:, :I] * sigmoid(h[:, :I])) * h[:, I:])
+        h = stb(h)
         u, v = h[:, :I], h[:, I:]
         sg = sigmoid(u)
         A = u * sg * v
@@ -373,7 +400,7 @@ def backward(X, W13, W2, idx, gate, dY, tokens=None, experts=None, mode="bf16"):
         dA = g * D
         du = dA * v * sg * (1.0 + u * (1.0 - sg))
         dv = dA * (u * sg)
-        dh = np.concatenate([du, dv], axis=1)
+        dh = stb(np.concatenate([du, dv], axis=1))
         dgate_rows = (A * D).sum(axis=1)
         dx_rows = qb(dh, 1) @ qb(W13[e], 1).T           # contraction over 2I
         for r, (aa, tt) in enumerate(zip(a, t)):
@@ -384,7 +411,7 @@ def backward(X, W13, W2, idx, gate, dY, tokens=None, experts=None, mode="bf16"):
             ei = exp_list.index(e)
             # contraction over the expert's tokens (column-wise blocks)
             dW13[ei] = qb(X[t], 0).T @ qb(dh, 0)
-            dW2[ei] = qb(A, 0).T @ qb(g * dYt, 0)
+            dW2[ei] = qb(A_saved, 0).T @ qb(stb(g * dYt), 0)
     return dict(dX=dX, dgate=dgate, dW13=dW13, dW2=dW2)
 
 

@@ -1,0 +1,111 @@
+"""MXFP8 (E4M3 / 32-element blocks / E8M0) and fp8_bwd (bf16 forward, MXFP8
+backward) modes of the layer on the GPU vs the float64 oracle, whose GEMM
+operands go through its own (bit-exact, separately tested) MXFP8 quantiser
+along each GEMM's contraction axis."""
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as O
+from workloads import CONFIGS, MoEConfig, make_inputs
+
+from _common import TOL_BF16, TOL_MXFP8, F32View, rel_err, to_device, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(cfg, inp, mode):
+    import torch
+    from mixture_experts_layer_18_gb300.layer import MoELayer
+    L = MoELayer(cfg.T, cfg.H, cfg.E, cfg.I, cfg.k, mode=mode)
+    io = L.empty_io()
+    dev = {k: to_device(v) for k, v in inp.items()}
+    L.route(dev["logits"])
+    L.forward(dev["X"], dev["W13"], dev["W2"], io["Y"])
+    L.backward(dev["dY"], dev["W13"], dev["W2"], io["dX"], io["dW13"], io["dW2"], io["dgate"])
+    torch.cuda.synchronize()
+    assert L.device_status() == 0
+    return L, io
+
+
+def _oracle_inputs(inp):
+    return {k: (F32View(v) if k != "logits" else v) for k, v in inp.items()}
+
+
+SMALL = [MoEConfig("mx_a", 512, 256, 8, 2, 256, "bf16"),
+         MoEConfig("mx_b", 700, 512, 16, 4, 256, "bf16"),
+         MoEConfig("mx_skew", 600, 256, 32, 4, 256, "bf16", skew=True)]
+
+
+@pytest.mark.parametrize("mode", ["mxfp8", "fp8_bwd"])
+@pytest.mark.parametrize("cfg", SMALL, ids=[c.name for c in SMALL])
+def test_small_shapes_full(cfg, mode):
+    inp = make_inputs(cfg)
+    L, io = _run(cfg, inp, mode)
+    oi = _oracle_inputs(inp)
+    idx, gate = O.route(inp["logits"], cfg.k)
+    Y, saved = O.forward(oi["X"], oi["W13"], oi["W2"], idx, gate, mode=mode, keep=True)
+    g = O.backward(oi["X"], oi["W13"], oi["W2"], idx, gate, oi["dY"], mode=mode)
+    tol_f = TOL_MXFP8 if mode == "mxfp8" else TOL_BF16
+    roa = L.row_of_assign.cpu().numpy()
+    h13 = to_f64(L.h13)
+    for e, s in saved.items():
+        assert rel_err(h13[roa[s["a"]]], s["h"]) <= tol_f, ("h13", e)
+    errs = {"Y": rel_err(to_f64(io["Y"]), Y)}
+    for k in ("dX", "dW13", "dW2", "dgate"):
+        errs[k] = rel_err(to_f64(io[k]), g[k])
+    assert errs["Y"] <= tol_f, errs
+    for k in ("dX", "dW13", "dW2", "dgate"):
+        assert errs[k] <= TOL_MXFP8, (k, errs)
+    # the quantised path really differs from the bf16 one (the test would not
+    # notice a silent bf16 fallback otherwise)
+    gb = O.backward(oi["X"], oi["W13"], oi["W2"], idx, gate, oi["dY"], mode="bf16")
+    assert rel_err(g["dW13"], gb["dW13"]) > 1e-3
+
+
+@pytest.mark.parametrize("mode", ["mxfp8", "fp8_bwd"])
+def test_full_size_235b_sampled(mode):
+    """235B layer shape.  The oracle is run on k=1 sub-batches: Y, dX and
+    d(gate) of a few tokens are rebuilt from one-row sub-problems of each of
+    their assignments (every quantised operand of those rows is row-wise or a
+    weight, so the sub-problem quantises exactly as the full layer does), and
+    dW of a few experts from sub-batches holding all of an expert's
+    assignments in ascending order (the token-axis blocks of the full layer)."""
+    from workloads import bf16_bits_to_f32
+    cfg = CONFIGS["235b_mxfp8"]
+    inp = make_inputs(cfg)
+    L, io = _run(cfg, inp, mode)
+    idx, gate = O.route(inp["logits"], cfg.k)
+    counts = np.bincount(idx.reshape(-1), minlength=cfg.E)
+
+    def f32(a):
+        return bf16_bits_to_f32(a) if a.dtype == np.uint16 else a
+
+    def sub(e, t, j):
+        one = np.zeros((len(t), 1), np.int32)
+        g = gate[t, j][:, None]
+        args = (f32(inp["X"][t]), f32(inp["W13"][e:e + 1]), f32(inp["W2"][e:e + 1]), one, g)
+        return O.forward(*args, mode=mode), O.backward(*args, f32(inp["dY"][t]), mode=mode)
+
+    rng = np.random.default_rng(2)
+    tokens = rng.choice(cfg.T, 1, replace=False)
+    Y = np.zeros((len(tokens), cfg.H))
+    dX = np.zeros((len(tokens), cfg.H))
+    dg = np.zeros((len(tokens), cfg.k))
+    for i, t in enumerate(tokens):
+        for j in range(cfg.k):
+            y, gb = sub(int(idx[t, j]), np.array([t]), np.array([j]))
+            Y[i] += y[0]
+            dX[i] += gb["dX"][0]
+            dg[i, j] = gb["dgate"][0, 0]
+    tol_f = TOL_MXFP8 if mode == "mxfp8" else TOL_BF16
+    errs = {"Y": rel_err(to_f64(io["Y"][tokens]), Y),
+            "dX": rel_err(to_f64(io["dX"][tokens]), dX),
+            "dgate": rel_err(to_f64(io["dgate"][tokens]), dg)}
+    for e in sorted({int(np.argmax(counts)), int(np.argmin(counts))}):
+        t, j = np.nonzero(idx == e)
+        _, gb = sub(e, t, j)
+        errs[f"dW13[{e}]"] = rel_err(to_f64(io["dW13"][e]), gb["dW13"][0])
+        errs[f"dW2[{e}]"] = rel_err(to_f64(io["dW2"][e]), gb["dW2"][0])
+    assert errs["Y"] <= tol_f, errs
+    for k, v in errs.items():
+        assert v <= TOL_MXFP8, (k, v, errs)

@@ -359,3 +359,36 @@ def test_mxfp8_colwise_groups_restart_at_group_start():
         cg, sg = O.quantize_mxfp8(x[go[g]:go[g + 1]], 0)
         assert np.array_equal(c[go[g]:go[g + 1]], cg)
         assert np.array_equal(sc[go[g] // 32:go[g + 1] // 32], sg)
+
+
+def test_bf16_round_matches_torch_conversion():
+    """The oracle's bf16 storage rounding equals torch's fp32 -> bf16
+    conversion (round to nearest even) on random and tie values."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(8)
+    x = (rng.standard_normal(50000) * np.exp(rng.uniform(-20, 20, 50000))).astype(np.float32)
+    ties = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 256 + 1], np.float32)
+    x = np.concatenate([x, ties])
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(O.bf16_round(x), want)
+    assert O.bf16_round(np.float32(1 + 2.0 ** -8)) == 1.0          # tie -> even
+    assert O.bf16_round(np.float32(1 + 3 * 2.0 ** -8)) == 1 + 2.0 ** -6
+
+
+def test_mxfp8_mode_equals_bf16_mode_on_representable_operands():
+    """E=1, k=1 with inputs and weights that MXFP8 represents exactly and
+    intermediates quantised from bf16: the mxfp8 forward equals the plain
+    forward computed on the same quantise-dequantised operands."""
+    rng = np.random.default_rng(9)
+    T, H, I = 4, 64, 32
+    def repr_(shape, axis):
+        return O.mx_qdq(O.bf16_round(rng.standard_normal(shape)), axis)
+    X = repr_((T, H), 1)
+    W13 = repr_((H, 2 * I), 0)[None]
+    W2 = repr_((I, H), 0)[None]
+    idx, gate = O.route(np.zeros((T, 1)), 1)
+    Ymx = O.forward(X, W13, W2, idx, gate, mode="mxfp8")
+    h = X @ W13[0]
+    A = O.silu(h[:, :I]) * h[:, I:]
+    Yref = O.mx_qdq(O.bf16_round(A), 1) @ W2[0]
+    assert np.allclose(Ymx, Yref, rtol=1e-12, atol=1e-12)
