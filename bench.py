@@ -35,7 +35,10 @@ import numpy as np  # noqa: E402
 
 from workloads import CONFIGS, make_inputs  # noqa: E402
 
-LAUNCHES_PER_STEP = 11   # route 3, forward 4, backward 4 (bf16 path)
+# kernels launched per step: route 3; forward 4 (+4 quantise passes in
+# mxfp8); backward 4 (+8 quantise passes and a second GEMM launch with MXFP8
+# gradients)
+LAUNCHES_PER_STEP = {"bf16": 11, "mxfp8": 24, "fp8_bwd": 20}
 CPU_SAMPLE_EXPERTS = 16   # cpu_baseline: all assignments of 16 experts
 REF_SAMPLE_EXPERTS = 1    # reference arm: one expert per step (rotating)
 
@@ -51,6 +54,10 @@ def _args():
     # smaller variants of the workload, for profiler captures
     p.add_argument("--tokens", type=int, default=None, help="override T")
     p.add_argument("--experts", type=int, default=None, help="override E")
+    p.add_argument("--mode", default="bf16", choices=["bf16", "mxfp8", "fp8_bwd"],
+                   help="GEMM precision (bf16; MXFP8 forward+backward; bf16 forward + MXFP8 backward)")
+    p.add_argument("--debug-flags", type=int, default=0,
+                   help="library debug flags (diagnosis runs only, e.g. 4 = split backward)")
     return p.parse_args()
 
 
@@ -248,7 +255,8 @@ def run_gpu(args):
         return torch.from_numpy(a).cuda()
 
     d = {k: dev(v) for k, v in inp.items()}
-    L = MoELayer(cfg.T, cfg.H, cfg.E, cfg.I, cfg.k, mode="bf16")
+    M.moe_set_debug(args.debug_flags, 0)
+    L = MoELayer(cfg.T, cfg.H, cfg.E, cfg.I, cfg.k, mode=args.mode)
     io = L.empty_io()
 
     def fwd():
@@ -349,32 +357,41 @@ def run_gpu(args):
     value = world * flops_step / (ms_step * 1e-3) / 1e12
     peaks, src = _peaks()
     peak = float(peaks["bf16_tflops"])
+    # MXFP8 contractions: measured bf16 peak x the nominal fp8 / bf16 ratio (2)
+    mx_b = args.mode in ("mxfp8", "fp8_bwd")
+    mx_f = args.mode == "mxfp8"
+    peak_b = peak * (2 if mx_b else 1)
+    peak_f = peak * (2 if mx_f else 1)
+    peak_note = f"{src} bf16_tflops (burst)" + (" x 2 (nominal fp8/bf16 ratio)" if mx_b else "")
     ach_b = cfg.bwd_flops() / (gemm_b * 1e-3) / 1e12
     ach_f = cfg.fwd_flops() / (gemm_f * 1e-3) / 1e12
-    traffic = _traffic("moe_gemm_kernel<bf16,256>/backward",
-                       ["mixture_experts_layer_18_gb300/csrc/gemm.cu",
-                        "mixture_experts_layer_18_gb300/csrc/common.cuh"])
+    traffic = None if mx_b else _traffic(
+        "moe_gemm_kernel<bf16,256,2>/backward",
+        ["mixture_experts_layer_18_gb300/csrc/gemm.cu",
+         "mixture_experts_layer_18_gb300/csrc/common.cuh"])
+    kname = ("moe_gemm_kernel<bf16,256,2> (co-scheduled backward GEMMs, one launch)" if not mx_b
+             else "MXFP8 backward: 2 GEMM launches + the 8 quantise passes between them")
     out = {
         "metric": "moe_layer_step_tflops", "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.mode,
         "data": "synthetic",
         "config": {"workload": _workload_desc(cfg), "T": cfg.T, "H": cfg.H, "E": cfg.E,
-                   "top_k": cfg.k, "I": cfg.I, "mode": "bf16",
+                   "top_k": cfg.k, "I": cfg.I, "mode": args.mode,
                    "flops_per_step": flops_step, "parallelism": "replicas",
                    "l2": "inputs larger than L2 (no flush)"},
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
         "fwd_tflops": cfg.fwd_flops() / (fwd_ms * 1e-3) / 1e12,
         "bwd_tflops": cfg.bwd_flops() / (bwd_ms * 1e-3) / 1e12,
-        "roofline": {"kernel": "moe_gemm_kernel<bf16,256> (co-scheduled backward GEMMs)",
-                     "bound": "tensor", "achieved": ach_b, "peak": peak, "unit": "TFLOP/s",
-                     "frac": ach_b / peak, "traffic": traffic,
-                     "peak_source": f"{src} bf16_tflops (burst)", "launch_ms": gemm_b},
-        "roofline_forward_gemms": {"achieved": ach_f, "peak": peak, "frac": ach_f / peak,
+        "roofline": {"kernel": kname,
+                     "bound": "tensor", "achieved": ach_b, "peak": peak_b, "unit": "TFLOP/s",
+                     "frac": ach_b / peak_b, "traffic": traffic,
+                     "peak_source": peak_note, "launch_ms": gemm_b},
+        "roofline_forward_gemms": {"achieved": ach_f, "peak": peak_f, "frac": ach_f / peak_f,
                                    "unit": "TFLOP/s", "launch_ms": gemm_f},
         "e2e": {"value": world * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": LAUNCHES_PER_STEP * K,
+        "gpu_launches": LAUNCHES_PER_STEP[args.mode] * K,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -216,8 +216,10 @@ const char* moe_status_string(moe_status s);
  * bumped, so the bounded wait runs out and MOE_ERR_TIMEOUT is reported.
  * Flag MOE_DEBUG_SINGLE_CTA runs the bf16 GEMMs with single-CTA 128-row
  * tiles instead of 256-row tiles over an SM pair (for A/B comparison).
+ * Flag MOE_DEBUG_SPLIT_BACKWARD runs the four bf16 gradient GEMMs as four
+ * consecutive launches instead of one co-scheduled launch (to time each).
  * Process-wide; not thread-safe against concurrent calls. */
-enum { MOE_DEBUG_NEVER_READY = 1, MOE_DEBUG_SINGLE_CTA = 2 };
+enum { MOE_DEBUG_NEVER_READY = 1, MOE_DEBUG_SINGLE_CTA = 2, MOE_DEBUG_SPLIT_BACKWARD = 4 };
 void moe_set_debug(int flags, int64_t wait_limit_ns);
 
 /* Timing hook for kernel-level measurement.  `start` and `stop` are

@@ -640,13 +640,26 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
     gw13.a_mn = gw13.b_mn = 1;
     gw13.a = x_perm; gw13.a_rows = rows; gw13.a_cols = d->H;
     gw13.b = dh13; gw13.b_rows = rows; gw13.b_cols = 2 * d->I;
-    L.nprob = 4;
-    L.prob[0] = gd;
-    L.prob[1] = gw2;
-    L.prob[2] = gx;
-    L.prob[3] = gw13;
-    MOE_TRY(launch_engine(L, s, &st));
-    if (st != MOE_OK) return st;
+    if (debug_flags() & MOE_DEBUG_SPLIT_BACKWARD) {
+      // one launch per gradient GEMM, in dependency order (diagnosis only)
+      gd.signal = 0;
+      gx.dep = gw13.dep = DEP_NONE;
+      const GemmDesc parts[4] = {gd, gw2, gx, gw13};
+      L.nprob = 1;
+      for (const GemmDesc& gp : parts) {
+        L.prob[0] = gp;
+        MOE_TRY(launch_engine(L, s, &st));
+        if (st != MOE_OK) return st;
+      }
+    } else {
+      L.nprob = 4;
+      L.prob[0] = gd;
+      L.prob[1] = gw2;
+      L.prob[2] = gx;
+      L.prob[3] = gw13;
+      MOE_TRY(launch_engine(L, s, &st));
+      if (st != MOE_OK) return st;
+    }
   } else {
     // TF32 reads K-major operands only: transposed token-axis copies, and the
     // weight-gradient GEMM of W13 runs after dh13 is complete.
