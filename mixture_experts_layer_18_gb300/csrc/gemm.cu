@@ -58,6 +58,8 @@ enum : int { DEP_NONE = 0, DEP_MBLOCK = 1, DEP_EXPERT = 2 };
 struct GemmProblem {
   CUtensorMap tmA;
   CUtensorMap tmB;
+  CUtensorMap tmO;   // bf16 outputs: 32 x 32 boxes, 64-byte swizzle (DW: 3-D [E, M, N])
+  CUtensorMap tmO2;  // FWD1: h13
   int kind, dep, signal;
   int a_mn, b_mn;    // operand stored M-/N-major (1) or K-major (0)
   int M, N, K;
@@ -103,8 +105,10 @@ struct Cfg {
   static constexpr int ATOM_BYTES = BK * 128;     // one MN-major column block
   static constexpr int SFA_BYTES = MX ? 512 : 0;              // one scale atom for A
   static constexpr int SFB_BYTES = MX ? (BNL / 128) * 512 : 0; // B atoms (BNL % 128 == 0)
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-  static constexpr int STAGES_RAW = (MX ? 204800 : 196608) / STAGE_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;        // multiple of 1024
+  static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;       // per stage, own region
+  static constexpr int TX_BYTES = (STAGE_BYTES + SF_BYTES) * PAIR;   // bytes per full barrier
+  static constexpr int STAGES_RAW = 196608 / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   // TMEM: NACC accumulators of BN columns; MXFP8 keeps one accumulator and a
   // 16-column scale slot per pipeline stage from column 256 on.
@@ -114,8 +118,10 @@ struct Cfg {
   static constexpr int KSTEPS = 4;                // MMAs per stage (32 bytes of K each)
   static constexpr int MN_KSTEP_BYTES = (32 / ES) * 128;  // MN-major advance per MMA
   static constexpr uint32_t FMT = ES == 2 ? 1u : (ES == 4 ? 2u : 0u);  // BF16 : TF32 : E4M3
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*bars*/ +
-                                    2 * (kMaxE + 1) * 4 + 64;
+  static constexpr int STG_BYTES = 4 * 4096;   // epilogue staging (4 warps x 2 x 2 KB)
+  static constexpr int SF_REGION = (STAGES * SF_BYTES + 255) / 256 * 256;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STG_BYTES + SF_REGION +
+                                    1024 /*align*/ + 256 /*bars*/ + 2 * (kMaxE + 1) * 4 + 64;
 };
 
 // ------------------------------------------------------------ tile decode
@@ -254,8 +260,8 @@ __device__ __forceinline__ void tma_load(void* dst, const CUtensorMap* m, int x,
 // leader CTA's full barrier, which the leader arms with the pair's bytes.
 template <class C>
 __device__ void producer_role(const EngineParams& P, const int* cum, int total, const int* s_po,
-                              const int* s_pt, int rank, uint8_t* stages, uint64_t* full,
-                              uint64_t* empty, const WaitCtl& wc) {
+                              const int* s_pt, int rank, uint8_t* stages, uint8_t* sfreg,
+                              uint64_t* full, uint64_t* empty, const WaitCtl& wc) {
   int it = 0;
   const int cl = blockIdx.x / C::PAIR, ncl = gridDim.x / C::PAIR;
   for (int t = cl; t < total; t += ncl) {
@@ -294,7 +300,7 @@ __device__ void producer_role(const EngineParams& P, const int* cum, int total, 
       uint8_t* sB = sA + C::A_BYTES;
       uint32_t fbar = 0;
       if constexpr (C::PAIR == 2) fbar = mapa_shared(smem_u32(&full[s]), 0);
-      if (rank == 0) mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES * C::PAIR);
+      if (rank == 0) mbar_arrive_expect_tx(&full[s], C::TX_BYTES);
       const int k0 = kb * C::BK;
       // A operand: M-major boxes (weight gradients) or one K-major box
       if (g.a_mn) {
@@ -323,7 +329,7 @@ __device__ void producer_role(const EngineParams& P, const int* cum, int total, 
       }
       if constexpr (C::MX) {
         // scale atoms: A's 128 rows x this K block, then B's column blocks
-        uint8_t* sSFA = sB + C::B_BYTES;
+        uint8_t* sSFA = sfreg + s * C::SF_BYTES;
         uint8_t* sSFB = sSFA + C::SFA_BYTES;
         bulk_load(sSFA,
                   g.sfa + ((size_t)(ti.m0 >> 7) * g.sfa_kg + ((ti.kbase + k0) >> 7)) * 512, 512,
@@ -357,7 +363,8 @@ __device__ void producer_role(const EngineParams& P, const int* cum, int total, 
 // MMA issuer: one thread of the (leader) CTA.
 template <class C>
 __device__ void mma_role(const EngineParams& P, const int* cum, int total, const int* s_po,
-                         const int* s_pt, uint8_t* stages, uint64_t* full, uint64_t* empty,
+                         const int* s_pt, uint8_t* stages, uint8_t* sfreg, uint64_t* full,
+                         uint64_t* empty,
                          uint64_t* tfull, uint64_t* tempty, uint64_t* drain, uint32_t tmem_base,
                          const WaitCtl& wc) {
   int it = 0, acc = 0;
@@ -394,7 +401,7 @@ __device__ void mma_role(const EngineParams& P, const int* cum, int total, const
       if constexpr (C::MX) {
         // scales of this stage into its TMEM slot: A at +0..3, B at +4..
         sf_slot = tmem_base + C::SF_COL0 + s * 16;
-        const uint32_t aS = aB + C::B_BYTES;
+        const uint32_t aS = smem_u32(sfreg) + s * C::SF_BYTES;
         tmem_cp_32x128b_x4(sf_slot, smem_desc_rows16(aS));
 #pragma unroll
         for (int j = 0; j < C::SFB_BYTES / 512; ++j)
@@ -468,23 +475,84 @@ __device__ __forceinline__ void load32(const Elt* src, float (&v)[32]) {
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// Staging of bf16 results (per epilogue warp: two 2 KB buffers of 32 rows x
+// 64 bytes, 64-byte swizzle: 16-byte chunk c of row r sits at chunk
+// c ^ ((r >> 1) & 3)), drained by TMA tensor stores.
+__device__ __forceinline__ void stage_bf16_row(uint8_t* buf, int r, const float (&v)[32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(buf + r * 64 + ((c ^ ((r >> 1) & 3)) << 4)) =
+        make_uint4(pack_bf16(v[8 * c + 0], v[8 * c + 1]), pack_bf16(v[8 * c + 2], v[8 * c + 3]),
+                   pack_bf16(v[8 * c + 4], v[8 * c + 5]), pack_bf16(v[8 * c + 6], v[8 * c + 7]));
+}
+
+template <typename Elt, int NV>
+__device__ __forceinline__ void load_raw(const Elt* src, uint4 (&d)[NV]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < NV; ++i) d[i] = s[i];
+}
+
+template <typename Elt, int NV>
+__device__ __forceinline__ void unpack_raw(const uint4 (&d)[NV], float (&v)[32]) {
+  if constexpr (sizeof(Elt) == 2) {
+#pragma unroll
+    for (int q = 0; q < NV; ++q) {
+      v[8 * q + 0] = bf16_lo(d[q].x); v[8 * q + 1] = bf16_hi(d[q].x);
+      v[8 * q + 2] = bf16_lo(d[q].y); v[8 * q + 3] = bf16_hi(d[q].y);
+      v[8 * q + 4] = bf16_lo(d[q].z); v[8 * q + 5] = bf16_hi(d[q].z);
+      v[8 * q + 6] = bf16_lo(d[q].w); v[8 * q + 7] = bf16_hi(d[q].w);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < NV; ++q) {
+      v[4 * q + 0] = __uint_as_float(d[q].x); v[4 * q + 1] = __uint_as_float(d[q].y);
+      v[4 * q + 2] = __uint_as_float(d[q].z); v[4 * q + 3] = __uint_as_float(d[q].w);
+    }
+  }
+}
+
 template <class C, typename Elt>
 __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, const int* s_po,
                               const int* s_pt, int rank, uint64_t* tfull, uint64_t* tempty,
-                              uint32_t tmem_base, volatile int* s_go, const WaitCtl& wc) {
+                              uint32_t tmem_base, volatile int* s_go, uint8_t* stg,
+                              const WaitCtl& wc) {
+  constexpr bool TS = sizeof(Elt) == 2;      // bf16 results leave through TMA stores
+  constexpr int NV = 32 * (int)sizeof(Elt) / 16;   // 16-byte vectors per 32 elements
   const int q = (threadIdx.x >> 5) & 3;      // TMEM lane quarter of this warp
   const int lane = threadIdx.x & 31;
   const int r = q * 32 + lane;               // tile row of this thread
   const bool leader = threadIdx.x == 64;     // first epilogue thread
   const int cl = blockIdx.x / C::PAIR, ncl = gridDim.x / C::PAIR;
+  uint8_t* sb0 = stg + q * 4096;
+  uint8_t* sb1 = sb0 + 2048;
   // the accumulator is released on the MMA-issuing CTA's barrier
   const uint32_t tempty_cl0 = C::PAIR == 2 ? mapa_shared(smem_u32(&tempty[0]), 0) : 0;
   const uint32_t tempty_cl1 = C::PAIR == 2 ? mapa_shared(smem_u32(&tempty[1]), 0) : 0;
+  // staging buffers free again (previous bulk stores have read them)
+  auto stage_begin = [&]() {
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+  };
+  // this warp's staged rows are visible to the bulk-copy engine
+  auto stage_end = [&]() {
+    fence_proxy_async_smem();
+    __syncwarp();
+  };
   int acc = 0;
   for (int t = cl; t < total; t += ncl) {
     const Tile ti = decode_tile<C>(P, cum, s_po, s_pt, t, rank);
     const GemmProblem& g = P.prob[ti.p];
     const int buf = acc % C::NACC;
+    const int yrow = ti.m0 + q * 32;         // first row of this warp's slice
+    // dSwiGLU inputs: the first chunk of h13 is fetched before the wait
+    uint4 pu[NV], pv[NV];
+    const Elt* h13a = nullptr;
+    if (ti.kind == GK_BWD_D && ti.valid) {
+      h13a = static_cast<const Elt*>(g.aux) + (size_t)(ti.m0 + r) * g.ld_aux + ti.n0;
+      load_raw<Elt, NV>(h13a, pu);
+      load_raw<Elt, NV>(h13a + g.I, pv);
+    }
     // One thread waits; the decision is shared so all 128 threads take the
     // same path through the named barriers below.  (s_go is indexed by
     // acc & 1 so a slow reader never sees the next tile's decision.)
@@ -506,12 +574,34 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
         tmem_ld32(taddr + c, v);               // u: gate half
         tmem_ld32(taddr + C::BN / 2 + c, w);   // v: up half
         if (h13) {
-          store32<Elt>(h13 + c, v);
-          store32<Elt>(h13 + g.I + c, w);
+          if constexpr (TS) {
+            stage_begin();
+            stage_bf16_row(sb0, lane, v);
+            stage_bf16_row(sb1, lane, w);
+            stage_end();
+            if (lane == 0) {
+              tma_store_2d(&g.tmO2, sb0, ti.n0 + c, yrow);
+              tma_store_2d(&g.tmO2, sb1, g.I + ti.n0 + c, yrow);
+              bulk_commit();
+            }
+          } else {
+            store32<Elt>(h13 + c, v);
+            store32<Elt>(h13 + g.I + c, w);
+          }
         }
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = v[i] / (1.f + __expf(-v[i])) * w[i];
-        store32<Elt>(outA + c, v);
+        if constexpr (TS) {
+          stage_begin();
+          stage_bf16_row(sb0, lane, v);
+          stage_end();
+          if (lane == 0) {
+            tma_store_2d(&g.tmO, sb0, ti.n0 + c, yrow);
+            bulk_commit();
+          }
+        } else {
+          store32<Elt>(outA + c, v);
+        }
       }
     } else if (ti.kind == GK_FWD2) {
       const int row = ti.m0 + r;
@@ -527,7 +617,17 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
         tmem_ld32(taddr + c, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= gt;
-        store32<Elt>(out + c, v);
+        if constexpr (TS) {
+          stage_begin();
+          stage_bf16_row(sb0, lane, v);
+          stage_end();
+          if (lane == 0) {
+            tma_store_2d(&g.tmO, sb0, ti.n0 + c, yrow);
+            bulk_commit();
+          }
+        } else {
+          store32<Elt>(out + c, v);
+        }
       }
     } else if (ti.kind == GK_BWD_D) {
       const int row = ti.m0 + r;
@@ -537,15 +637,18 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
         a = -1;
       }
       const float gt = a >= 0 ? g.gate[a] : 0.f;
-      const Elt* h13 = static_cast<const Elt*>(g.aux) + (size_t)row * g.ld_aux + ti.n0;
       Elt* dh = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
       float part = 0.f;
 #pragma unroll 1
       for (int c = 0; c < C::BN; c += 32) {
         float D[32];
+        unpack_raw<Elt, NV>(pu, v);            // u of this chunk
+        unpack_raw<Elt, NV>(pv, w);            // v of this chunk
+        if (c + 32 < C::BN) {                  // fetch the next chunk while this one runs
+          load_raw<Elt, NV>(h13a + c + 32, pu);
+          load_raw<Elt, NV>(h13a + g.I + c + 32, pv);
+        }
         tmem_ld32(taddr + c, D);
-        load32<Elt>(h13 + c, v);               // u
-        load32<Elt>(h13 + g.I + c, w);         // v
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float u = v[i], vv = w[i];
@@ -556,8 +659,20 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
           v[i] = a >= 0 ? dA * vv * sg * (1.f + u * (1.f - sg)) : 0.f;   // du
           w[i] = a >= 0 ? dA * si : 0.f;                                  // dv
         }
-        store32<Elt>(dh + c, v);
-        store32<Elt>(dh + g.I + c, w);
+        if constexpr (TS) {
+          stage_begin();
+          stage_bf16_row(sb0, lane, v);
+          stage_bf16_row(sb1, lane, w);
+          stage_end();
+          if (lane == 0) {
+            tma_store_2d(&g.tmO, sb0, ti.n0 + c, yrow);
+            tma_store_2d(&g.tmO, sb1, g.I + ti.n0 + c, yrow);
+            bulk_commit();
+          }
+        } else {
+          store32<Elt>(dh + c, v);
+          store32<Elt>(dh + g.I + c, w);
+        }
       }
       g.partial[(size_t)row * g.nt + ti.ntile] = a >= 0 ? part : 0.f;
     } else if (ti.kind == GK_BWD_DX) {
@@ -566,7 +681,17 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
 #pragma unroll 1
       for (int c = 0; c < C::BN; c += 32) {
         tmem_ld32(taddr + c, v);
-        store32<Elt>(out + c, v);
+        if constexpr (TS) {
+          stage_begin();
+          stage_bf16_row(sb0, lane, v);
+          stage_end();
+          if (lane == 0) {
+            tma_store_2d(&g.tmO, sb0, ti.n0 + c, yrow);
+            bulk_commit();
+          }
+        } else {
+          store32<Elt>(out + c, v);
+        }
       }
     } else {  // GK_DW
       const bool valid = ti.m0 + r < g.M;
@@ -579,7 +704,18 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0.f;
         }
-        if (valid) store32<Elt>(out + c, v);
+        if constexpr (TS) {
+          // rows past M are outside the [E, M, N] view: the store clips them
+          stage_begin();
+          stage_bf16_row(sb0, lane, v);
+          stage_end();
+          if (lane == 0) {
+            tma_store_3d(&g.tmO, sb0, ti.n0 + c, ti.m0 + q * 32, ti.e);
+            bulk_commit();
+          }
+        } else {
+          if (valid) store32<Elt>(out + c, v);
+        }
       }
     }
     tc_fence_before();
@@ -589,7 +725,10 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       else mbar_arrive(&tempty[buf]);
     }
     if (g.signal && ti.valid) {
-      // Publish this tile's rows to TMA readers in other CTAs.
+      // Publish this tile's rows to TMA readers in other CTAs: the bulk
+      // stores complete, then a release on the m-block's counter.
+      if (TS && lane == 0) bulk_wait_all();
+      __syncwarp();
       fence_proxy_async_global();
       __threadfence();
       epi_bar();
@@ -597,6 +736,8 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
     }
     ++acc;
   }
+  if (TS && lane == 0) bulk_wait_all();    // every store done before the CTA exits
+  __syncwarp();
 }
 
 // ----------------------------------------------------------------- kernel
@@ -606,7 +747,9 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint8_t* stg = smem + C::STAGES * C::STAGE_BYTES;   // 1024-aligned (stage sizes are)
+  uint8_t* sfreg = stg + C::STG_BYTES;                 // MXFP8 scale atoms per stage
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sfreg + C::SF_REGION);
   uint64_t* full = bars;
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
@@ -615,7 +758,7 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
   int* s_go = abort_flag + 1;           // [2]
-  int* s_po = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + 256);
+  int* s_po = reinterpret_cast<int*>(sfreg + C::SF_REGION + 256);
   int* s_pt = s_po + (kMaxE + 1);       // pair tiles before expert e (PAIR == 2)
 
   const int warp = threadIdx.x >> 5;
@@ -692,15 +835,16 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
 
   if (warp == 0) {
     if ((threadIdx.x & 31) == 0)
-      producer_role<C>(P, cum, total, s_po, s_pt, rank, stages, full, empty, wc);
+      producer_role<C>(P, cum, total, s_po, s_pt, rank, stages, sfreg, full, empty, wc);
     __syncwarp();
   } else if (warp == 1) {
     if ((threadIdx.x & 31) == 0 && rank == 0)
-      mma_role<C>(P, cum, total, s_po, s_pt, stages, full, empty, tfull, tempty, drain, tmem_base,
-                  wc);
+      mma_role<C>(P, cum, total, s_po, s_pt, stages, sfreg, full, empty, tfull, tempty, drain,
+                  tmem_base, wc);
     __syncwarp();
   } else {
-    epilogue_role<C, Out>(P, cum, total, s_po, s_pt, rank, tfull, tempty, tmem_base, s_go, wc);
+    epilogue_role<C, Out>(P, cum, total, s_po, s_pt, rank, tfull, tempty, tmem_base, s_go, stg,
+                          wc);
   }
   tc_fence_before();
   __syncthreads();
@@ -755,6 +899,32 @@ bool make_tmap(CUtensorMap* m, const void* base, int elem_bytes, int64_t rows, i
   return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 output views for the epilogue's bulk stores: 32 x 32 boxes, 64-byte
+// swizzle (matching the staging layout).  2-D [rows, cols] or 3-D [E, M, N].
+bool make_tmap_out(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tmap_out3(CUtensorMap* m, void* base, int64_t E, int64_t M, int64_t N) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)E};
+  cuuint64_t strides[2] = {(cuuint64_t)N * 2, (cuuint64_t)(M * N * 2)};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int sm_count() {
@@ -874,6 +1044,15 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
     ok = ok && (b_mn ? make_tmap(&g.tmB, d.b, es, d.b_rows, d.b_cols, ATOM, BK)
                      : make_tmap(&g.tmB, d.b, es, d.b_rows, d.b_cols, BK,
                                  d.kind == GK_FWD1 ? L.BN / 2 : L.BN / pair));
+    if (es != 4 && d.out) {   // bf16 results: bulk-store views of the outputs
+      if (d.kind == GK_DW) {
+        if (d.ld_out != d.N) { *st = MOE_ERR_UNSUPPORTED; return cudaSuccess; }
+        ok = make_tmap_out3(&g.tmO, d.out, L.E, d.M, d.N);
+      } else {
+        ok = make_tmap_out(&g.tmO, d.out, L.max_rows, d.ld_out);
+        if (ok && d.out2) ok = make_tmap_out(&g.tmO2, d.out2, L.max_rows, d.ld_out2);
+      }
+    }
     if (!ok) { *st = MOE_ERR_CUDA; return cudaSuccess; }
     tile_bound += d.kind == GK_DW ? (int64_t)L.E * ((d.M + 127) / 128) * g.nt : mblocks_max * g.nt;
   }
