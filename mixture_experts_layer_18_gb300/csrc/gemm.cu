@@ -85,8 +85,9 @@ struct EngineParams {
   int nprob;
   int E;
   const int32_t* padded_offsets;
-  int32_t* ready;
-  int ready_target;
+  int32_t* ready;         // per-m-block counters, then one total at ready_all_index
+  int ready_target;       // publications per m-block (n-tiles of the signalling problem)
+  int ready_all_index;
   int32_t* status;
   unsigned long long wait_ns;
 };
@@ -264,17 +265,26 @@ __device__ void producer_role(const EngineParams& P, const int* cum, int total, 
                               uint64_t* full, uint64_t* empty, const WaitCtl& wc) {
   int it = 0;
   const int cl = blockIdx.x / C::PAIR, ncl = gridDim.x / C::PAIR;
+  // ready[nmb] counts every published (m-block, n-tile) of the signalling
+  // problem; once it reaches nmb * ready_target all dependencies hold and
+  // later tiles skip their per-m-block checks.
+  const int nmb = s_po[P.E] / 128;
+  int32_t* const ready_all = P.ready + P.ready_all_index;
+  bool all_ready = false;
   for (int t = cl; t < total; t += ncl) {
     const Tile ti = decode_tile<C>(P, cum, s_po, s_pt, t, rank);
     const GemmProblem& g = P.prob[ti.p];
-    if (g.dep == DEP_MBLOCK) {
-      if (ti.valid && !wait_counter(P.ready + ti.mb, P.ready_target, wc)) break;
-      fence_proxy_async_global();
-    } else if (g.dep == DEP_EXPERT) {
-      bool ok = true;
-      for (int mb = s_po[ti.e] / 128; ok && mb < s_po[ti.e + 1] / 128; ++mb)
-        ok = wait_counter(P.ready + mb, P.ready_target, wc);
-      if (!ok) break;
+    if (g.dep != DEP_NONE && !all_ready) {
+      if ((int64_t)ld_acquire(ready_all) >= (int64_t)nmb * P.ready_target) {
+        all_ready = true;
+      } else if (g.dep == DEP_MBLOCK) {
+        if (ti.valid && !wait_counter(P.ready + ti.mb, P.ready_target, wc)) break;
+      } else {
+        bool ok = true;
+        for (int mb = s_po[ti.e] / 128; ok && mb < s_po[ti.e + 1] / 128; ++mb)
+          ok = wait_counter(P.ready + mb, P.ready_target, wc);
+        if (!ok) break;
+      }
       fence_proxy_async_global();
     }
     // B column segments staged by this CTA: (first column or row, count)
@@ -732,7 +742,10 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       fence_proxy_async_global();
       __threadfence();
       epi_bar();
-      if (leader) red_release_add(P.ready + ti.mb, 1);
+      if (leader) {
+        red_release_add(P.ready + ti.mb, 1);
+        red_release_add(P.ready + P.ready_all_index, 1);
+      }
     }
     ++acc;
   }
@@ -994,6 +1007,7 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
   P.padded_offsets = L.padded_offsets;
   P.ready = L.ready;
   P.ready_target = L.ready_target;
+  P.ready_all_index = (int)((L.max_rows + 127) / 128);
   P.status = L.status;
   P.wait_ns = L.wait_ns;
   const int es = L.elem_bytes;

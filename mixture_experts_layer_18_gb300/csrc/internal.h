@@ -88,7 +88,7 @@ struct EngineLaunch {
   int BN;                      // 64, 128 or 256
   const int32_t* padded_offsets;
   int64_t max_rows;
-  int32_t* ready;
+  int32_t* ready;              // [(max_rows + 127) / 128 + 1] readiness counters
   int ready_target;
   int32_t* status;
   uint64_t wait_ns;

@@ -146,7 +146,7 @@ BwdWs bwd_ws(const moe_dims* d) {
   w.dh13 = o; o += align256(rows * 2 * d->I * es);
   w.dxp = o; o += align256(rows * d->H * es);
   w.partial = o; o += align256(rows * w.nt_d * sizeof(float));
-  w.ready = o; o += align256(((rows + 127) / 128) * sizeof(int32_t));
+  w.ready = o; o += align256(((rows + 127) / 128 + 1) * sizeof(int32_t));
   const bool t = d->mode == MOE_F32;
   const size_t lt = (size_t)ld_t(d) * es;
   w.act_t = o; o += t ? align256(lt * d->I) : 0;
@@ -567,7 +567,7 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
   MOE_TRY(launch_gather_grad(dY, dy_perm, dyg_perm, d->H, es, d->top_k, n_assign,
                              r->assign_of_row, r->gate, r->padded_offsets, d->E, rows, dev_status,
                              s));
-  MOE_TRY(cudaMemsetAsync(ready, 0, ((rows + 127) / 128) * sizeof(int32_t), s));
+  MOE_TRY(cudaMemsetAsync(ready, 0, ((rows + 127) / 128 + 1) * sizeof(int32_t), s));
 
   if (mx_bwd(d)) {
     EventScope timing(MOE_WS_BACKWARD, s);
