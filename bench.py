@@ -1,6 +1,7 @@
 #!/usr/bin/env python
 """Benchmark of the dropless MoE expert layer on GB300: one step = route +
-forward + backward of one layer over one batch of synthetic tokens.
+forward + backward (down to d(logits) of the router) of one layer over one
+batch of synthetic tokens.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 235b]
   python bench.py --impl reference ...      # the float64 CPU oracle arm
@@ -37,8 +38,8 @@ from workloads import CONFIGS, make_inputs  # noqa: E402
 
 # kernels launched per step: route 3; forward 4 (+4 quantise passes in
 # mxfp8); backward 4 (+8 quantise passes and a second GEMM launch with MXFP8
-# gradients)
-LAUNCHES_PER_STEP = {"bf16": 11, "mxfp8": 24, "fp8_bwd": 20}
+# gradients); router backward 1
+LAUNCHES_PER_STEP = {"bf16": 12, "mxfp8": 25, "fp8_bwd": 21}   # incl. the router backward
 CPU_SAMPLE_EXPERTS = 16   # cpu_baseline: all assignments of 16 experts
 REF_SAMPLE_EXPERTS = 1    # reference arm: one expert per step (rotating)
 
@@ -263,8 +264,11 @@ def run_gpu(args):
         L.route(d["logits"])
         L.forward(d["X"], d["W13"], d["W2"], io["Y"])
 
+    dlogits = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device="cuda")
+
     def bwd():
         L.backward(d["dY"], d["W13"], d["W2"], io["dX"], io["dW13"], io["dW2"], io["dgate"])
+        L.route_backward(io["dgate"], dlogits)
 
     def step():
         fwd()

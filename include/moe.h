@@ -153,6 +153,19 @@ moe_status moe_route_noalloc(const moe_dims* dims, const float* logits,
                              const moe_route_out* out, int32_t* dev_status,
                              void* stream);
 
+/* Router backward: d(logits) from d(gate) through the renormalised top-k
+ * softmax, the selection held fixed.  For a selected expert i of token t,
+ * gate_i = exp(l_i) / sum_{j in top-k} exp(l_j), so
+ *   dlogits[t, i] = gate_i * (dgate_i - sum_j gate_j * dgate_j),
+ * and every unselected expert gets 0 (the step upstream of moe_backward's
+ * d(gate); [MM] "How does the fused kernel work?": the trainable backward).
+ *   route    moe_route output (topk_idx and gate are read).
+ *   dgate    float [T, top_k] (device), e.g. from moe_backward.
+ *   dlogits  float [T, E] (device), fully overwritten. */
+moe_status moe_route_backward(const moe_dims* dims, const moe_route_out* route,
+                              const float* dgate, float* dlogits,
+                              int32_t* dev_status, void* stream);
+
 /* Forward of the expert layer ([MM] "How does the fused kernel work?";
  * [TE] "Optimisation 1" and "Optimisation 2"):
  *   X_perm = rows of X in expert-major order (pad rows 0)

@@ -19,7 +19,7 @@ __all__ = [
     "MOE_FP8_BWD", "MOE_WS_ROUTE", "MOE_WS_FORWARD", "MOE_WS_BACKWARD",
     "MOE_DEBUG_NEVER_READY", "MOE_DEBUG_SINGLE_CTA", "MOE_DEBUG_SPLIT_BACKWARD", "moe_dims", "moe_route_out", "moe_saved_layout",
     "lib", "header_functions", "moe_max_rows", "moe_workspace_size",
-    "moe_saved_layout_of", "moe_route", "moe_route_noalloc", "moe_forward", "moe_backward",
+    "moe_saved_layout_of", "moe_route", "moe_route_noalloc", "moe_route_backward", "moe_forward", "moe_backward",
     "moe_quantize_mxfp8", "moe_status_string", "moe_set_debug", "moe_set_gemm_events",
     "MoEError",
 ]
@@ -66,6 +66,7 @@ _SIGS = {
     "moe_saved_layout_of": (_c_int, [_PD, ctypes.POINTER(moe_saved_layout)]),
     "moe_route": (_c_int, [_PD, _vp, _PR, _vp, _c_size, _vp, _vp]),
     "moe_route_noalloc": (_c_int, [_PD, _vp, _PR, _vp, _vp]),
+    "moe_route_backward": (_c_int, [_PD, _PR, _vp, _vp, _vp, _vp]),
     "moe_forward": (_c_int, [_PD, _vp, _vp, _vp, _PR, _vp, _vp, _c_size, _vp, _c_size, _vp, _vp]),
     "moe_backward": (_c_int, [_PD, _vp, _vp, _vp, _PR, _vp, _c_size, _vp, _vp, _vp, _vp, _vp,
                               _c_size, _vp, _vp]),
@@ -124,6 +125,11 @@ def moe_route(d, logits, out, ws, ws_bytes, dev_status, stream) -> int:
 
 def moe_route_noalloc(d, logits, out, dev_status, stream) -> int:
     return lib().moe_route_noalloc(ctypes.byref(d), logits, ctypes.byref(out), dev_status, stream)
+
+
+def moe_route_backward(d, route, dgate, dlogits, dev_status, stream) -> int:
+    return lib().moe_route_backward(ctypes.byref(d), ctypes.byref(route), dgate, dlogits,
+                                    dev_status, stream)
 
 
 def moe_forward(d, X, W13, W2, route, Y, saved, saved_bytes, ws, ws_bytes, dev_status,

@@ -18,6 +18,9 @@ constexpr int kMaxTopK = 32;
 // route.cu
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* topk_idx,
                          float* gate, int32_t* block_hist, int32_t* status, cudaStream_t s);
+cudaError_t launch_route_backward(const int32_t* topk_idx, const float* gate, const float* dgate,
+                                  int T, int E, int k, float* dlogits, int32_t* status,
+                                  cudaStream_t s);
 cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int64_t max_rows,
                            const int32_t* block_hist_in, int32_t* block_base, int32_t* counts,
                            int32_t* offsets, int32_t* padded_offsets, int32_t* row_of_assign,

@@ -432,6 +432,15 @@ moe_status moe_route(const moe_dims* d, const float* logits, const moe_route_out
   return MOE_OK;
 }
 
+moe_status moe_route_backward(const moe_dims* d, const moe_route_out* r, const float* dgate,
+                              float* dlogits, int32_t* dev_status, void* stream) {
+  if (!dims_ok(d) || !route_ok(r, d->T) || !aligned16(dev_status)) return MOE_ERR_INVALID_ARG;
+  if (d->T > 0 && (!aligned16(dgate) || !aligned16(dlogits))) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(launch_route_backward(r->topk_idx, r->gate, dgate, d->T, d->E, d->top_k, dlogits,
+                                dev_status, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
 moe_status moe_forward(const moe_dims* d, const void* X, const void* W13, const void* W2,
                        const moe_route_out* r, void* Y, void* saved, size_t saved_bytes,
                        void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {

@@ -200,7 +200,73 @@ __global__ void __launch_bounds__(256) scatter_kernel(
   }
 }
 
+// Router backward: with the selection held fixed, gate_j = exp(l_j) /
+// sum_{i in top-k} exp(l_i), so d(logit) of a selected expert i is
+// g_i * (dg_i - sum_j g_j dg_j) and zero for every other expert.  One warp
+// per token; lane j < k holds slot j; the row of E logits is written once,
+// coalesced.
+template <int VPL>
+__global__ void __launch_bounds__(kRouteThreads) route_backward_kernel(
+    const int32_t* __restrict__ topk_idx, const float* __restrict__ gate,
+    const float* __restrict__ dgate, int T, int E, int k, float* __restrict__ dlogits,
+    int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+    const size_t base = (size_t)t * k;
+    const float g = lane < k ? gate[base + lane] : 0.f;
+    const float dg = lane < k ? dgate[base + lane] : 0.f;
+    int e = lane < k ? topk_idx[base + lane] : -1;
+    if (lane < k && (e < 0 || e >= E)) {
+      report(status, MOE_ERR_BAD_INDEX);
+      e = -1;
+    }
+    float inner = g * dg;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) inner += __shfl_xor_sync(0xffffffffu, inner, off);
+    const float dl = g * (dg - inner);
+    float out[VPL];
+#pragma unroll
+    for (int q = 0; q < VPL; ++q) out[q] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int ej = __shfl_sync(0xffffffffu, e, j);
+      const float dj = __shfl_sync(0xffffffffu, dl, j);
+      if (ej >= 0 && (ej & 31) == lane) {
+#pragma unroll
+        for (int q = 0; q < VPL; ++q)
+          if (q == (ej >> 5)) out[q] = dj;
+      }
+    }
+    float* row = dlogits + (size_t)t * E;
+#pragma unroll
+    for (int q = 0; q < VPL; ++q) {
+      const int ee = q * 32 + lane;
+      if (ee < E) row[ee] = out[q];
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_route_backward(const int32_t* topk_idx, const float* gate, const float* dgate,
+                                  int T, int E, int k, float* dlogits, int32_t* status,
+                                  cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int blocks = (T + (kRouteThreads / 32) - 1) / (kRouteThreads / 32);
+  const int grid = blocks < 4096 ? blocks : 4096;
+  const int vpl = (E + 31) / 32;
+  if (vpl <= 1)
+    route_backward_kernel<1><<<grid, kRouteThreads, 0, s>>>(topk_idx, gate, dgate, T, E, k, dlogits, status);
+  else if (vpl <= 4)
+    route_backward_kernel<4><<<grid, kRouteThreads, 0, s>>>(topk_idx, gate, dgate, T, E, k, dlogits, status);
+  else if (vpl <= 8)
+    route_backward_kernel<8><<<grid, kRouteThreads, 0, s>>>(topk_idx, gate, dgate, T, E, k, dlogits, status);
+  else if (vpl <= 16)
+    route_backward_kernel<16><<<grid, kRouteThreads, 0, s>>>(topk_idx, gate, dgate, T, E, k, dlogits, status);
+  else
+    route_backward_kernel<32><<<grid, kRouteThreads, 0, s>>>(topk_idx, gate, dgate, T, E, k, dlogits, status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* topk_idx,
                          float* gate, int32_t* block_hist, int32_t* /*status*/,

@@ -11,7 +11,8 @@ import torch
 
 from . import (MOE_BF16, MOE_F32, MOE_FP8_BWD, MOE_MXFP8, MOE_OK, MOE_WS_BACKWARD,
                MOE_WS_FORWARD, MOE_WS_ROUTE, MoEError, moe_backward, moe_dims, moe_forward,
-               moe_max_rows, moe_route, moe_route_out, moe_saved_layout_of, moe_workspace_size)
+               moe_max_rows, moe_route, moe_route_backward, moe_route_out, moe_saved_layout_of,
+               moe_workspace_size)
 
 MODES = {"f32": MOE_F32, "bf16": MOE_BF16, "mxfp8": MOE_MXFP8, "fp8_bwd": MOE_FP8_BWD}
 
@@ -105,6 +106,12 @@ class MoELayer:
                           _ptr(self.status), _stream(stream))
         if rc != MOE_OK:
             raise MoEError(rc, "moe_backward")
+
+    def route_backward(self, dgate, dlogits, stream=None):
+        rc = moe_route_backward(self.dims, self.route_out, _ptr(dgate), _ptr(dlogits),
+                                _ptr(self.status), _stream(stream))
+        if rc != MOE_OK:
+            raise MoEError(rc, "moe_route_backward")
 
     # --------------------------------------------------------- allocation
     def empty_io(self):
