@@ -332,6 +332,26 @@ def run_gpu(args):
     fwd_ms = timed(fwd, K)
     bwd_ms = timed(bwd, K)
 
+    # ---- the pages' full-layer measure: 2 x forward + backward with full
+    # activation checkpointing (a forward that keeps nothing, then the
+    # recomputing forward and the backward), captured as one CUDA graph
+    def full_layer():
+        L.route(d["logits"])
+        L.forward(d["X"], d["W13"], d["W2"], io["Y"], save=False)
+        L.forward(d["X"], d["W13"], d["W2"], io["Y"], save=True)
+        bwd()
+
+    full_layer()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        full_layer()
+    graph.replay()
+    torch.cuda.synchronize()
+    full_ms = timed(graph.replay, K)
+    if L.device_status() != 0:
+        raise RuntimeError(f"device status {L.device_status()} after graph replays")
+
     # ---- end to end: pinned host inputs in, results out, every step
     h_in = {k: d[k].cpu().pin_memory() for k in ("logits", "X", "dY")}
     h_out = {k: torch.empty(io[k].shape, dtype=io[k].dtype, pin_memory=True)
@@ -351,11 +371,11 @@ def run_gpu(args):
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
 
     # ---- max over ranks
-    t = torch.tensor([ms_step, e2e_ms, fwd_ms, bwd_ms, gemm_b, gemm_f], device="cuda",
+    t = torch.tensor([ms_step, e2e_ms, fwd_ms, bwd_ms, gemm_b, gemm_f, full_ms], device="cuda",
                      dtype=torch.float64)
     if world > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_step, e2e_ms, fwd_ms, bwd_ms, gemm_b, gemm_f = t.tolist()
+    ms_step, e2e_ms, fwd_ms, bwd_ms, gemm_b, gemm_f, full_ms = t.tolist()
 
     flops_step = cfg.fwd_flops() + cfg.bwd_flops()
     value = world * flops_step / (ms_step * 1e-3) / 1e12
@@ -385,6 +405,10 @@ def run_gpu(args):
                    "flops_per_step": flops_step, "parallelism": "replicas",
                    "l2": "inputs larger than L2 (no flush)"},
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+        "full_layer": {"ms": full_ms, "what": "2 x forward + backward (full activation "
+                       "checkpointing), replayed as one CUDA graph",
+                       "tflops": world * (2 * cfg.fwd_flops() + cfg.bwd_flops()) /
+                       (full_ms * 1e-3) / 1e12},
         "fwd_tflops": cfg.fwd_flops() / (fwd_ms * 1e-3) / 1e12,
         "bwd_tflops": cfg.bwd_flops() / (bwd_ms * 1e-3) / 1e12,
         "roofline": {"kernel": kname,

@@ -92,8 +92,14 @@ class MoELayer:
         if rc != MOE_OK:
             raise MoEError(rc, "moe_route")
 
-    def forward(self, X, W13, W2, Y, stream=None):
-        rc = moe_forward(self.dims, _ptr(X), _ptr(W13), _ptr(W2), self.route_out, _ptr(Y),
+    def forward(self, X, W13, W2, Y, stream=None, save=None):
+        """save: None = the layer's setting; False = inference / checkpointed
+        first pass (h13 not kept); True = keep h13 for moe_backward."""
+        dims = self.dims
+        if save is not None and bool(save) != bool(self.dims.save_for_backward):
+            dims = moe_dims(self.dims.T, self.dims.H, self.dims.E, self.dims.I, self.dims.top_k,
+                            self.dims.mode, 1 if save else 0)
+        rc = moe_forward(dims, _ptr(X), _ptr(W13), _ptr(W2), self.route_out, _ptr(Y),
                          _ptr(self.saved), self.saved.numel(), _ptr(self.ws_fwd),
                          self.ws_fwd.numel(), _ptr(self.status), _stream(stream))
         if rc != MOE_OK:
