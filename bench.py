@@ -203,6 +203,24 @@ def _traffic(kernel, src_files):
     return None
 
 
+def max_over_ranks(values, world, device):
+    """Element-wise maximum of per-rank timings (the slowest replica sets the
+    whole job's time); the identity for a single process."""
+    import torch
+    if world <= 1:
+        return list(values)
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(flops_per_step, world, ms_step):
+    """Whole-job TFLOP/s: every replica runs one step of flops_per_step in the
+    (max over ranks) step time."""
+    return world * flops_per_step / (ms_step * 1e-3) / 1e12
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -371,14 +389,11 @@ def run_gpu(args):
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
 
     # ---- max over ranks
-    t = torch.tensor([ms_step, e2e_ms, fwd_ms, bwd_ms, gemm_b, gemm_f, full_ms], device="cuda",
-                     dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_step, e2e_ms, fwd_ms, bwd_ms, gemm_b, gemm_f, full_ms = t.tolist()
+    ms_step, e2e_ms, fwd_ms, bwd_ms, gemm_b, gemm_f, full_ms = max_over_ranks(
+        [ms_step, e2e_ms, fwd_ms, bwd_ms, gemm_b, gemm_f, full_ms], world, "cuda")
 
     flops_step = cfg.fwd_flops() + cfg.bwd_flops()
-    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    value = job_throughput(flops_step, world, ms_step)
     peaks, src = _peaks()
     peak = float(peaks["bf16_tflops"])
     # MXFP8 contractions: measured bf16 peak x the nominal fp8 / bf16 ratio (2)
