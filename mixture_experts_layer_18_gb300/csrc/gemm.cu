@@ -32,9 +32,10 @@
 // [E*2I, H], W2^T [E*H, I], S^T [M, rows], G^T [N, rows]); TF32 MMAs read
 // K-major operands only, so the fp32 mode uses those copies throughout.
 //
-// CTA layout (192 threads, one CTA per SM): warp 0 lane 0 issues TMA loads,
-// warp 1 owns TMEM and lane 0 issues tcgen05.mma, warps 2..5 run the
-// epilogue (warp w reads TMEM lanes 32*(w%4) .. +31, i.e. tile rows).
+// CTA layout (one CTA per SM): warp 0 lane 0 issues TMA loads, warp 1 owns
+// TMEM and lane 0 issues tcgen05.mma, warps 2..5 run the epilogue (warp w
+// reads TMEM lanes 32*(w%4) .. +31, i.e. tile rows); block-scaled pairs have
+// warps 2..9, two per lane quarter, each on half of the tile's columns.
 // bf16 problems run on SM pairs (clusters of 2, cta_group::2): one 256-row
 // tile per pair, each CTA staging its 128 rows of A and half of B, so a
 // pipeline stage is 32 KB per CTA (6 stages) instead of 48 KB (4 stages) and
@@ -74,9 +75,10 @@ struct GemmProblem {
   const int32_t* assign_of_row;
   int n_assign;      // valid assignment indices are [0, n_assign)
   float* partial;
-  // MXFP8 operands: E8M0 scale atoms (512 B per 128 MN indices x 128 K)
-  const uint8_t* sfa;
-  const uint8_t* sfb;
+  // MXFP8 operands: E8M0 scale atoms (512 B per 128 MN indices x 128 K),
+  // read through [atoms * 4, 128]-byte views: atom i is rows 4i .. 4i + 3.
+  CUtensorMap tmSFA;
+  CUtensorMap tmSFB;
   int sfa_kg, sfb_kg;  // K groups of 128 in each operand's 2-D view
 };
 
@@ -104,12 +106,22 @@ struct Cfg {
   static constexpr int A_BYTES = 128 * 128;       // 128 rows x 128 bytes
   static constexpr int B_BYTES = BNL * 128;
   static constexpr int ATOM_BYTES = BK * 128;     // one MN-major column block
-  static constexpr int SFA_BYTES = MX ? 512 : 0;              // one scale atom for A
-  static constexpr int SFB_BYTES = MX ? (BNL / 128) * 512 : 0; // B atoms (BNL % 128 == 0)
+  // scale atoms per stage: A's 128 rows, and B's scales for all BN columns
+  // of the MMA (each CTA of a pair needs every column's scale in its TMEM)
+  static constexpr int SFA_BYTES = MX ? 512 : 0;
+  static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;        // multiple of 1024
   static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;       // per stage, own region
   static constexpr int TX_BYTES = (STAGE_BYTES + SF_BYTES) * PAIR;   // bytes per full barrier
-  static constexpr int STAGES_RAW = 196608 / STAGE_BYTES;
+  // Epilogue warps: 4 (one per TMEM lane quarter), or 8 for block-scaled
+  // pairs, whose single accumulator keeps the MMAs idle while it drains
+  // (two warps per quarter, each taking half of the tile's columns).
+  static constexpr int EPI_WARPS = MX && PAIR == 2 ? 8 : 4;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int STG_BYTES = EPI_WARPS * 4096;   // epilogue staging (2 x 2 KB per warp)
+  static constexpr int FIXED_BYTES = STG_BYTES + 1024 /*align*/ + 256 /*bars*/ +
+                                     2 * (kMaxE + 1) * 4 + 512 /*row partials*/ + 64 + 256;
+  static constexpr int STAGES_RAW = (232448 - FIXED_BYTES) / (STAGE_BYTES + SF_BYTES);
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   // TMEM: NACC accumulators of BN columns; MXFP8 keeps one accumulator and a
   // 16-column scale slot per pipeline stage from column 256 on.
@@ -119,10 +131,11 @@ struct Cfg {
   static constexpr int KSTEPS = 4;                // MMAs per stage (32 bytes of K each)
   static constexpr int MN_KSTEP_BYTES = (32 / ES) * 128;  // MN-major advance per MMA
   static constexpr uint32_t FMT = ES == 2 ? 1u : (ES == 4 ? 2u : 0u);  // BF16 : TF32 : E4M3
-  static constexpr int STG_BYTES = 4 * 4096;   // epilogue staging (4 warps x 2 x 2 KB)
   static constexpr int SF_REGION = (STAGES * SF_BYTES + 255) / 256 * 256;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STG_BYTES + SF_REGION +
-                                    1024 /*align*/ + 256 /*bars*/ + 2 * (kMaxE + 1) * 4 + 64;
+                                    1024 /*align*/ + 256 /*bars*/ + 2 * (kMaxE + 1) * 4 + 512 + 64;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+  static_assert(!MX || SF_COL0 + STAGES * 16 <= 512, "TMEM scale slots");
 };
 
 // ------------------------------------------------------------ tile decode
@@ -338,21 +351,23 @@ __device__ void producer_role(const EngineParams& P, const int* cum, int total, 
                         fbar);
       }
       if constexpr (C::MX) {
-        // scale atoms: A's 128 rows x this K block, then B's column blocks
+        // scale atoms: A's 128 rows x this K block (rows past the expert or
+        // M read atom 0: their results are dropped), then the atoms of every
+        // B column of the MMA -- for FWD1 the gate block, then the up block.
         uint8_t* sSFA = sfreg + s * C::SF_BYTES;
         uint8_t* sSFB = sSFA + C::SFA_BYTES;
-        bulk_load(sSFA,
-                  g.sfa + ((size_t)(ti.m0 >> 7) * g.sfa_kg + ((ti.kbase + k0) >> 7)) * 512, 512,
-                  &full[s]);
+        const int amb = ti.valid ? (ti.m0 >> 7) : 0;
+        tma_load<C>(sSFA, &g.tmSFA, 0, (amb * g.sfa_kg + ((ti.kbase + k0) >> 7)) * 4, &full[s],
+                    fbar);
         const int kidx = g.b_mn ? yb : ti.kbase + k0;
+        const int nseg = ti.kind == GK_FWD1 ? 2 : 1;
         int ai = 0;
-        for (int sg = 0; sg < 2; ++sg) {
-          const int seg = sg ? seg1 : seg0;
-          if (seg < 0) continue;
-          for (int j = 0; j < seglen / 128; ++j, ++ai) {
+        for (int sg = 0; sg < nseg; ++sg) {
+          const int seg = ti.n0 + (sg ? g.I : 0);
+          for (int j = 0; j < C::BN / nseg / 128; ++j, ++ai) {
             const int mn = (g.b_mn ? 0 : yrow) + seg + 128 * j;
-            bulk_load(sSFB + ai * 512,
-                      g.sfb + ((size_t)(mn >> 7) * g.sfb_kg + (kidx >> 7)) * 512, 512, &full[s]);
+            tma_load<C>(sSFB + ai * 512, &g.tmSFB, 0, ((mn >> 7) * g.sfb_kg + (kidx >> 7)) * 4,
+                        &full[s], fbar);
           }
         }
       }
@@ -412,10 +427,13 @@ __device__ void mma_role(const EngineParams& P, const int* cum, int total, const
         // scales of this stage into its TMEM slot: A at +0..3, B at +4..
         sf_slot = tmem_base + C::SF_COL0 + s * 16;
         const uint32_t aS = smem_u32(sfreg) + s * C::SF_BYTES;
-        tmem_cp_32x128b_x4(sf_slot, smem_desc_rows16(aS));
 #pragma unroll
-        for (int j = 0; j < C::SFB_BYTES / 512; ++j)
-          tmem_cp_32x128b_x4(sf_slot + 4 + 4 * j, smem_desc_rows16(aS + 512 + 512 * j));
+        for (int j = 0; j < 1 + C::SFB_BYTES / 512; ++j) {
+          if constexpr (C::PAIR == 2)
+            tmem_cp_32x128b_x4_pair(sf_slot + 4 * j, smem_desc_rows16(aS + 512 * j));
+          else
+            tmem_cp_32x128b_x4(sf_slot + 4 * j, smem_desc_rows16(aS + 512 * j));
+        }
       }
 #pragma unroll
       for (int kk = 0; kk < C::KSTEPS; ++kk) {
@@ -423,7 +441,10 @@ __device__ void mma_role(const EngineParams& P, const int* cum, int total, const
                                  : smem_desc_sw128(aA + kk * 32, 16, 1024);
         const uint64_t bd = b_mn ? smem_desc_sw128(aB + kk * C::MN_KSTEP_BYTES, C::ATOM_BYTES, 1024)
                                  : smem_desc_sw128(aB + kk * 32, 16, 1024);
-        if constexpr (C::MX)
+        if constexpr (C::MX && C::PAIR == 2)
+          mma_mxf8_pair(d, ad, bd, idesc | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), sf_slot,
+                        sf_slot + 4, (kb | kk) != 0);
+        else if constexpr (C::MX)
           mma_mxf8(d, ad, bd, idesc | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), sf_slot,
                    sf_slot + 4, (kb | kk) != 0);
         else if constexpr (C::PAIR == 2)
@@ -483,7 +504,10 @@ __device__ __forceinline__ void load32(const Elt* src, float (&v)[32]) {
   }
 }
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+template <int NTHREADS>
+__device__ __forceinline__ void epi_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NTHREADS) : "memory");
+}
 
 // Staging of bf16 results (per epilogue warp: two 2 KB buffers of 32 rows x
 // 64 bytes, 64-byte swizzle: 16-byte chunk c of row r sits at chunk
@@ -526,15 +550,19 @@ template <class C, typename Elt>
 __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, const int* s_po,
                               const int* s_pt, int rank, uint64_t* tfull, uint64_t* tempty,
                               uint32_t tmem_base, volatile int* s_go, uint8_t* stg,
-                              const WaitCtl& wc) {
+                              float* s_part, const WaitCtl& wc) {
   constexpr bool TS = sizeof(Elt) == 2;      // bf16 results leave through TMA stores
   constexpr int NV = 32 * (int)sizeof(Elt) / 16;   // 16-byte vectors per 32 elements
+  constexpr int ET = C::EPI_WARPS * 32;      // epilogue threads
+  constexpr int NH = C::EPI_WARPS / 4;       // column parts per tile row (1 or 2)
+  const int ew = (threadIdx.x >> 5) - 2;     // epilogue warp
   const int q = (threadIdx.x >> 5) & 3;      // TMEM lane quarter of this warp
+  const int h = ew >> 2;                     // column part of this warp
   const int lane = threadIdx.x & 31;
   const int r = q * 32 + lane;               // tile row of this thread
   const bool leader = threadIdx.x == 64;     // first epilogue thread
   const int cl = blockIdx.x / C::PAIR, ncl = gridDim.x / C::PAIR;
-  uint8_t* sb0 = stg + q * 4096;
+  uint8_t* sb0 = stg + ew * 4096;
   uint8_t* sb1 = sb0 + 2048;
   // the accumulator is released on the MMA-issuing CTA's barrier
   const uint32_t tempty_cl0 = C::PAIR == 2 ? mapa_shared(smem_u32(&tempty[0]), 0) : 0;
@@ -555,19 +583,22 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
     const GemmProblem& g = P.prob[ti.p];
     const int buf = acc % C::NACC;
     const int yrow = ti.m0 + q * 32;         // first row of this warp's slice
+    // accumulator columns [cb, cb + cw) of this warp (FWD1: of each half)
+    const int cw = (ti.kind == GK_FWD1 ? C::BN / 2 : C::BN) / NH;
+    const int cb = h * cw;
     // dSwiGLU inputs: the first chunk of h13 is fetched before the wait
     uint4 pu[NV], pv[NV];
     const Elt* h13a = nullptr;
     if (ti.kind == GK_BWD_D && ti.valid) {
       h13a = static_cast<const Elt*>(g.aux) + (size_t)(ti.m0 + r) * g.ld_aux + ti.n0;
-      load_raw<Elt, NV>(h13a, pu);
-      load_raw<Elt, NV>(h13a + g.I, pv);
+      load_raw<Elt, NV>(h13a + cb, pu);
+      load_raw<Elt, NV>(h13a + g.I + cb, pv);
     }
-    // One thread waits; the decision is shared so all 128 threads take the
-    // same path through the named barriers below.  (s_go is indexed by
+    // One thread waits; the decision is shared so all epilogue threads take
+    // the same path through the named barriers below.  (s_go is indexed by
     // acc & 1 so a slow reader never sees the next tile's decision.)
     if (leader) s_go[acc & 1] = wait_bar_p<C>(&tfull[buf], (acc / C::NACC) & 1, wc) ? 1 : 0;
-    epi_bar();
+    epi_bar<ET>();
     if (!s_go[acc & 1]) break;
     tc_fence_after();
     __syncwarp();
@@ -580,7 +611,7 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       Elt* outA = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
       Elt* h13 = g.out2 ? static_cast<Elt*>(g.out2) + (size_t)row * g.ld_out2 + ti.n0 : nullptr;
 #pragma unroll 1
-      for (int c = 0; c < C::BN / 2; c += 32) {
+      for (int c = cb; c < cb + cw; c += 32) {
         tmem_ld32(taddr + c, v);               // u: gate half
         tmem_ld32(taddr + C::BN / 2 + c, w);   // v: up half
         if (h13) {
@@ -623,7 +654,7 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       const float gt = a >= 0 ? g.gate[a] : 0.f;
       Elt* out = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
 #pragma unroll 1
-      for (int c = 0; c < C::BN; c += 32) {
+      for (int c = cb; c < cb + cw; c += 32) {
         tmem_ld32(taddr + c, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= gt;
@@ -650,11 +681,11 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       Elt* dh = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
       float part = 0.f;
 #pragma unroll 1
-      for (int c = 0; c < C::BN; c += 32) {
+      for (int c = cb; c < cb + cw; c += 32) {
         float D[32];
         unpack_raw<Elt, NV>(pu, v);            // u of this chunk
         unpack_raw<Elt, NV>(pv, w);            // v of this chunk
-        if (c + 32 < C::BN) {                  // fetch the next chunk while this one runs
+        if (c + 32 < cb + cw) {                // fetch the next chunk while this one runs
           load_raw<Elt, NV>(h13a + c + 32, pu);
           load_raw<Elt, NV>(h13a + g.I + c + 32, pv);
         }
@@ -684,12 +715,19 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
           store32<Elt>(dh + g.I + c, w);
         }
       }
-      g.partial[(size_t)row * g.nt + ti.ntile] = a >= 0 ? part : 0.f;
+      if constexpr (NH == 2) {
+        // the second column part hands its sum to the first (fixed order)
+        if (h == 1) s_part[r] = part;
+        epi_bar<ET>();
+        if (h == 0) g.partial[(size_t)row * g.nt + ti.ntile] = a >= 0 ? part + s_part[r] : 0.f;
+      } else {
+        g.partial[(size_t)row * g.nt + ti.ntile] = a >= 0 ? part : 0.f;
+      }
     } else if (ti.kind == GK_BWD_DX) {
       const int row = ti.m0 + r;
       Elt* out = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
 #pragma unroll 1
-      for (int c = 0; c < C::BN; c += 32) {
+      for (int c = cb; c < cb + cw; c += 32) {
         tmem_ld32(taddr + c, v);
         if constexpr (TS) {
           stage_begin();
@@ -707,7 +745,7 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       const bool valid = ti.m0 + r < g.M;
       Elt* out = static_cast<Elt*>(g.out) + ((size_t)ti.e * g.M + ti.m0 + r) * g.ld_out + ti.n0;
 #pragma unroll 1
-      for (int c = 0; c < C::BN; c += 32) {
+      for (int c = cb; c < cb + cw; c += 32) {
         if (ti.nk > 0) {
           tmem_ld32(taddr + c, v);
         } else {
@@ -741,7 +779,7 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       __syncwarp();
       fence_proxy_async_global();
       __threadfence();
-      epi_bar();
+      epi_bar<ET>();
       if (leader) {
         red_release_add(P.ready + ti.mb, 1);
         red_release_add(P.ready + P.ready_all_index, 1);
@@ -755,7 +793,8 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
 
 // ----------------------------------------------------------------- kernel
 template <typename In, typename Out, int BN, int PAIR>
-__global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant__ EngineParams P) {
+__global__ void __launch_bounds__(Cfg<In, BN, PAIR>::THREADS, 1)
+    moe_gemm_kernel(const __grid_constant__ EngineParams P) {
   using C = Cfg<In, BN, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -773,6 +812,7 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
   int* s_go = abort_flag + 1;           // [2]
   int* s_po = reinterpret_cast<int*>(sfreg + C::SF_REGION + 256);
   int* s_pt = s_po + (kMaxE + 1);       // pair tiles before expert e (PAIR == 2)
+  float* s_part = reinterpret_cast<float*>(s_pt + (kMaxE + 1));   // [128] row partials
 
   const int warp = threadIdx.x >> 5;
   const int rank = PAIR == 2 ? (int)cluster_ctarank() : 0;
@@ -783,7 +823,7 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4 * PAIR);  // one arrival per epilogue warp of the pair
+      mbar_init(&tempty[b], C::EPI_WARPS * PAIR);  // one arrival per epilogue warp of the pair
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -799,6 +839,10 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
     for (int p = 0; p < P.nprob; ++p) {
       tma_prefetch_desc(&P.prob[p].tmA);
       tma_prefetch_desc(&P.prob[p].tmB);
+      if constexpr (C::MX) {
+        tma_prefetch_desc(&P.prob[p].tmSFA);
+        tma_prefetch_desc(&P.prob[p].tmSFB);
+      }
     }
   }
   __syncthreads();
@@ -857,7 +901,7 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
     __syncwarp();
   } else {
     epilogue_role<C, Out>(P, cum, total, s_po, s_pt, rank, tfull, tempty, tmem_base, s_go, stg,
-                          wc);
+                          s_part, wc);
   }
   tc_fence_before();
   __syncthreads();
@@ -928,6 +972,20 @@ bool make_tmap_out(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// MXFP8 scale atoms as a [bytes / 128, 128] uint8 tensor, boxes of one
+// 512-byte atom (4 x 128), no swizzle.
+bool make_tmap_sf(CUtensorMap* m, const void* base, int64_t bytes) {
+  auto enc = encode_fn();
+  if (!enc || bytes <= 0 || bytes % 512) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)(bytes / 128)};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, 4};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_tmap_out3(CUtensorMap* m, void* base, int64_t E, int64_t M, int64_t N) {
   auto enc = encode_fn();
   if (!enc) return false;
@@ -967,7 +1025,7 @@ cudaError_t launch_typed(const EngineParams& P, int64_t tile_bound, cudaStream_t
   if constexpr (PAIR == 1) {
     int grid = sm_count();
     if (tile_bound < grid) grid = (int)(tile_bound < 1 ? 1 : tile_bound);
-    kern<<<grid, 192, C::SMEM_BYTES, s>>>(P);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(P);
     return cudaGetLastError();
   } else {
     cudaLaunchConfig_t cfg = {};
@@ -976,7 +1034,7 @@ cudaError_t launch_typed(const EngineParams& P, int64_t tile_bound, cudaStream_t
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(192, 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
     cfg.attrs = attr;
@@ -1012,9 +1070,10 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
   P.wait_ns = L.wait_ns;
   const int es = L.elem_bytes;
   const int BK = 128 / es, ATOM = 128 / es;
-  // bf16 runs 256-row tiles over an SM pair (B split in halves of >= 64
-  // columns); TF32 and narrow tiles run on single CTAs.
-  const int pair = es == 2 && L.BN >= 128 && !(debug_flags() & MOE_DEBUG_SINGLE_CTA) ? 2 : 1;
+  // bf16 and MXFP8 run 256-row tiles over an SM pair (B split in halves of
+  // >= 64 columns); TF32 and narrow tiles run on single CTAs.
+  const int pair = (es == 2 || es == 1) && L.BN >= 128 && !(debug_flags() & MOE_DEBUG_SINGLE_CTA)
+                       ? 2 : 1;
   int64_t tile_bound = 0;
   const int64_t mblocks_max = (L.max_rows + 127) / 128;
   for (int p = 0; p < L.nprob; ++p) {
@@ -1040,11 +1099,13 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
     g.assign_of_row = d.assign_of_row;
     g.n_assign = d.n_assign;
     g.partial = d.partial;
-    g.sfa = d.sfa;
-    g.sfb = d.sfb;
     g.sfa_kg = d.sfa_kg;
     g.sfb_kg = d.sfb_kg;
-    if (es == 1 && (!d.sfa || !d.sfb)) { *st = MOE_ERR_INVALID_ARG; return cudaSuccess; }
+    if (es == 1 && !(make_tmap_sf(&g.tmSFA, d.sfa, d.sfa_bytes) &&
+                     make_tmap_sf(&g.tmSFB, d.sfb, d.sfb_bytes))) {
+      *st = MOE_ERR_INVALID_ARG;
+      return cudaSuccess;
+    }
     const bool a_mn = d.a_mn != 0;
     const bool b_mn = d.b_mn != 0;
     if ((a_mn || b_mn) && es == 4) { *st = MOE_ERR_UNSUPPORTED; return cudaSuccess; }  // TF32: K-major only
@@ -1082,6 +1143,7 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
       case 64: return launch_typed<__nv_bfloat16, __nv_bfloat16, 64, 1>(P, tile_bound, s);
     }
   } else if (es == 1) {   // MXFP8 operands, bf16 outputs
+    if (L.BN == 256 && pair == 2) return launch_typed<uint8_t, __nv_bfloat16, 256, 2>(P, tile_bound, s);
     if (L.BN == 256) return launch_typed<uint8_t, __nv_bfloat16, 256, 1>(P, tile_bound, s);
   } else if (es == 4) {
     switch (L.BN) {

@@ -80,6 +80,7 @@ struct GemmDesc {
   float* partial;
   const uint8_t* sfa;          // MXFP8: scale atoms of A / B (quant.cu layout 1)
   const uint8_t* sfb;
+  int64_t sfa_bytes, sfb_bytes;  // size of each scale-atom array (multiple of 512)
   int sfa_kg, sfb_kg;          // K groups of 128 in each operand's 2-D view
 };
 

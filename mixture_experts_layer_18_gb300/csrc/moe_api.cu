@@ -92,7 +92,7 @@ int64_t ld_t(const moe_dims* d) { return (max_rows(d) + 31) / 32 * 32; }
 
 // MXFP8: one quantised operand = E4M3 codes + tensor-core scale atoms.
 struct MxBuf {
-  size_t q, sf;
+  size_t q, sf, sf_bytes;
 };
 int64_t rows_pad(const moe_dims* d) { return (max_rows(d) + 127) / 128 * 128; }
 // codes of an [R, C] operand (R padded to 128 for the atoms)
@@ -101,7 +101,8 @@ MxBuf mx_carve(size_t& o, size_t R, size_t Rp, size_t C) {
   b.q = o;
   o += align256(R * C);
   b.sf = o;
-  o += align256(Rp * C / 32);
+  b.sf_bytes = Rp * C / 32;
+  o += align256(b.sf_bytes);
   return b;
 }
 
@@ -221,9 +222,10 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 struct Mx {
   const void* q;
   const uint8_t* sf;
+  int64_t sf_bytes;
 };
 Mx mx_at(char* base, const MxBuf& b) {
-  return Mx{base + b.q, reinterpret_cast<const uint8_t*>(base + b.sf)};
+  return Mx{base + b.q, reinterpret_cast<const uint8_t*>(base + b.sf), (int64_t)b.sf_bytes};
 }
 
 cudaError_t quant_rows(const void* src, int64_t R, int C, const Mx& m, int32_t* st, cudaStream_t s) {
@@ -257,10 +259,10 @@ moe_status forward_mx(const moe_dims* d, const void* W13, const void* W2, const 
     GemmDesc& g = L.prob[0];
     g = GemmDesc{};
     g.kind = GK_FWD1;
-    g.a = x.q; g.a_rows = rows; g.a_cols = H; g.sfa = x.sf; g.sfa_kg = H / 128;
+    g.a = x.q; g.a_rows = rows; g.a_cols = H; g.sfa = x.sf; g.sfa_bytes = x.sf_bytes; g.sfa_kg = H / 128;
     g.b_mn = 1;
     g.b = w13.q; g.b_rows = (int64_t)E * H; g.b_cols = 2 * I; g.b_expert_rows = H;
-    g.sfb = w13.sf; g.sfb_kg = (int)((int64_t)E * H / 128);
+    g.sfb = w13.sf; g.sfb_bytes = w13.sf_bytes; g.sfb_kg = (int)((int64_t)E * H / 128);
     g.N = 2 * I; g.K = H; g.I = I;
     g.out = act; g.ld_out = I;
     g.out2 = d->save_for_backward ? h13 : nullptr; g.ld_out2 = 2 * I;
@@ -273,10 +275,10 @@ moe_status forward_mx(const moe_dims* d, const void* W13, const void* W2, const 
     GemmDesc& g = L.prob[0];
     g = GemmDesc{};
     g.kind = GK_FWD2;
-    g.a = a.q; g.a_rows = rows; g.a_cols = I; g.sfa = a.sf; g.sfa_kg = I / 128;
+    g.a = a.q; g.a_rows = rows; g.a_cols = I; g.sfa = a.sf; g.sfa_bytes = a.sf_bytes; g.sfa_kg = I / 128;
     g.b_mn = 1;
     g.b = w2.q; g.b_rows = (int64_t)E * I; g.b_cols = H; g.b_expert_rows = I;
-    g.sfb = w2.sf; g.sfb_kg = (int)((int64_t)E * I / 128);
+    g.sfb = w2.sf; g.sfb_bytes = w2.sf_bytes; g.sfb_kg = (int)((int64_t)E * I / 128);
     g.N = H; g.K = I;
     g.out = zg; g.ld_out = H;
     g.gate = r->gate; g.assign_of_row = r->assign_of_row; g.n_assign = d->T * d->top_k;
@@ -321,9 +323,9 @@ moe_status backward_mx(const moe_dims* d, const void* W13, const void* W2,
     GemmDesc& gd = L.prob[0];
     gd = GemmDesc{};
     gd.kind = GK_BWD_D;
-    gd.a = dy.q; gd.a_rows = rows; gd.a_cols = H; gd.sfa = dy.sf; gd.sfa_kg = H / 128;
+    gd.a = dy.q; gd.a_rows = rows; gd.a_cols = H; gd.sfa = dy.sf; gd.sfa_bytes = dy.sf_bytes; gd.sfa_kg = H / 128;
     gd.b = w2r.q; gd.b_rows = (int64_t)E * I; gd.b_cols = H; gd.b_expert_rows = I;
-    gd.sfb = w2r.sf; gd.sfb_kg = H / 128;
+    gd.sfb = w2r.sf; gd.sfb_bytes = w2r.sf_bytes; gd.sfb_kg = H / 128;
     gd.N = I; gd.K = H; gd.I = I;
     gd.out = dh13; gd.ld_out = 2 * I;
     gd.aux = h13; gd.ld_aux = 2 * I;
@@ -333,8 +335,8 @@ moe_status backward_mx(const moe_dims* d, const void* W13, const void* W2,
     gw2 = GemmDesc{};
     gw2.kind = GK_DW;
     gw2.a_mn = gw2.b_mn = 1;
-    gw2.a = actc.q; gw2.a_rows = rows; gw2.a_cols = I; gw2.sfa = actc.sf; gw2.sfa_kg = kgt;
-    gw2.b = dygc.q; gw2.b_rows = rows; gw2.b_cols = H; gw2.sfb = dygc.sf; gw2.sfb_kg = kgt;
+    gw2.a = actc.q; gw2.a_rows = rows; gw2.a_cols = I; gw2.sfa = actc.sf; gw2.sfa_bytes = actc.sf_bytes; gw2.sfa_kg = kgt;
+    gw2.b = dygc.q; gw2.b_rows = rows; gw2.b_cols = H; gw2.sfb = dygc.sf; gw2.sfb_bytes = dygc.sf_bytes; gw2.sfb_kg = kgt;
     gw2.M = I; gw2.N = H;
     gw2.out = dW2; gw2.ld_out = H;
     MOE_TRY(launch_engine(L, s, &st));
@@ -349,17 +351,17 @@ moe_status backward_mx(const moe_dims* d, const void* W13, const void* W2,
     GemmDesc& gx = L.prob[0];
     gx = GemmDesc{};
     gx.kind = GK_BWD_DX;
-    gx.a = dh13r.q; gx.a_rows = rows; gx.a_cols = 2 * I; gx.sfa = dh13r.sf; gx.sfa_kg = 2 * I / 128;
+    gx.a = dh13r.q; gx.a_rows = rows; gx.a_cols = 2 * I; gx.sfa = dh13r.sf; gx.sfa_bytes = dh13r.sf_bytes; gx.sfa_kg = 2 * I / 128;
     gx.b = w13r.q; gx.b_rows = (int64_t)E * H; gx.b_cols = 2 * I; gx.b_expert_rows = H;
-    gx.sfb = w13r.sf; gx.sfb_kg = 2 * I / 128;
+    gx.sfb = w13r.sf; gx.sfb_bytes = w13r.sf_bytes; gx.sfb_kg = 2 * I / 128;
     gx.N = H; gx.K = 2 * I;
     gx.out = dxp; gx.ld_out = H;
     GemmDesc& gw = L.prob[1];
     gw = GemmDesc{};
     gw.kind = GK_DW;
     gw.a_mn = gw.b_mn = 1;
-    gw.a = xpc.q; gw.a_rows = rows; gw.a_cols = H; gw.sfa = xpc.sf; gw.sfa_kg = kgt;
-    gw.b = dh13c.q; gw.b_rows = rows; gw.b_cols = 2 * I; gw.sfb = dh13c.sf; gw.sfb_kg = kgt;
+    gw.a = xpc.q; gw.a_rows = rows; gw.a_cols = H; gw.sfa = xpc.sf; gw.sfa_bytes = xpc.sf_bytes; gw.sfa_kg = kgt;
+    gw.b = dh13c.q; gw.b_rows = rows; gw.b_cols = 2 * I; gw.sfb = dh13c.sf; gw.sfb_bytes = dh13c.sf_bytes; gw.sfb_kg = kgt;
     gw.M = H; gw.N = 2 * I;
     gw.out = dW13; gw.ld_out = 2 * I;
     MOE_TRY(launch_engine(L, s, &st));

@@ -18,70 +18,105 @@ namespace moe {
 
 namespace {
 
-constexpr int kRouteThreads = 256;                      // 8 warps
-constexpr int kTokPerWarp = kRouteTokPerBlock / (kRouteThreads / 32);
+constexpr int kBwdThreads = 256;
 
-// One warp per token.  Lane l holds logits l, l+32, l+64, ... in registers.
-// k rounds of a warp arg-max pick the largest remaining logit, ties to the
-// lower expert index (a total order for NaN-free input).  Slot j of the
-// result is the j-th pick.  Also builds this block's expert histogram.
+// Block shape of the router: 32 warps (4 tokens each, side by side) while a
+// token's logits fit in 4 registers per lane; larger E keeps 8 warps and
+// fewer tokens in flight per warp so the logits stay in registers.
+template <int VPL> struct RouteShape {
+  static constexpr int THREADS = VPL <= 8 ? 1024 : 256;
+  static constexpr int NT = kRouteTokPerBlock / (THREADS / 32);   // tokens per warp
+  static constexpr int ILP = VPL <= 4 ? 4 : (VPL <= 8 ? 2 : 1);  // processed side by side
+};
+
+// One warp per token; ILP tokens of a warp are processed side by side
+// (independent shuffle chains, so their latencies overlap).  Lane l holds
+// logits l, l+32, l+64, ... of each token in registers.  k rounds of a warp
+// arg-max pick the largest remaining logit, ties to the lower expert index
+// (a total order for NaN-free input).  Slot j of the result is the j-th
+// pick.  Also builds this block's expert histogram.
 template <int VPL>
-__global__ void __launch_bounds__(kRouteThreads) route_kernel(
+__global__ void __launch_bounds__(RouteShape<VPL>::THREADS) route_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,
     float* __restrict__ gate, int32_t* __restrict__ block_hist, int nb) {
+  constexpr int NT = RouteShape<VPL>::NT, ILP = RouteShape<VPL>::ILP;
   __shared__ int hist[kMaxE];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = 0; i < kTokPerWarp; ++i) {
-    const int t = blockIdx.x * kRouteTokPerBlock + warp * kTokPerWarp + i;
-    if (t >= T) break;
-    const float* row = logits + (size_t)t * E;
-    float v[VPL];
-    uint32_t taken = 0;  // bit q: element q*32+lane chosen already or absent
+  for (int g = 0; g < NT; g += ILP) {
+    const int t0 = blockIdx.x * kRouteTokPerBlock + warp * NT + g;
+    if (t0 >= T) break;
+    float v[ILP][VPL];
+    uint32_t taken[ILP];   // bit q: element q*32+lane chosen already or absent
 #pragma unroll
-    for (int q = 0; q < VPL; ++q) {
-      const int e = q * 32 + lane;
-      v[q] = e < E ? __ldg(row + e) : 0.f;
-      if (e >= E) taken |= 1u << q;
-    }
-    float sel_v = 0.f;
-    int sel_e = 0;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int be = INT_MAX;
+    for (int i = 0; i < ILP; ++i) {
+      const int t = t0 + i;
+      taken[i] = 0;
 #pragma unroll
       for (int q = 0; q < VPL; ++q) {
         const int e = q * 32 + lane;
-        if (!((taken >> q) & 1u) && (v[q] > bv || (v[q] == bv && e < be))) {
-          bv = v[q];
-          be = e;
+        v[i][q] = (e < E && t < T) ? __ldg(logits + (size_t)t * E + e) : 0.f;
+        if (e >= E) taken[i] |= 1u << q;
+      }
+    }
+    float sel_v[ILP];
+    int sel_e[ILP];
+#pragma unroll
+    for (int i = 0; i < ILP; ++i) {
+      sel_v[i] = 0.f;
+      sel_e[i] = 0;
+    }
+    for (int j = 0; j < k; ++j) {
+      float bv[ILP];
+      int be[ILP];
+#pragma unroll
+      for (int i = 0; i < ILP; ++i) {
+        bv[i] = -INFINITY;
+        be[i] = INT_MAX;
+#pragma unroll
+        for (int q = 0; q < VPL; ++q) {
+          const int e = q * 32 + lane;
+          if (!((taken[i] >> q) & 1u) && (v[i][q] > bv[i] || (v[i][q] == bv[i] && e < be[i]))) {
+            bv[i] = v[i][q];
+            be[i] = e;
+          }
         }
       }
 #pragma unroll
       for (int off = 16; off; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
+#pragma unroll
+        for (int i = 0; i < ILP; ++i) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv[i], off);
+          const int oe = __shfl_xor_sync(0xffffffffu, be[i], off);
+          if (ov > bv[i] || (ov == bv[i] && oe < be[i])) {
+            bv[i] = ov;
+            be[i] = oe;
+          }
         }
       }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (lane == j) {
-        sel_v = bv;
-        sel_e = be;
+#pragma unroll
+      for (int i = 0; i < ILP; ++i) {
+        if ((be[i] & 31) == lane) taken[i] |= 1u << (be[i] >> 5);
+        if (lane == j) {
+          sel_v[i] = bv[i];
+          sel_e[i] = be[i];
+        }
       }
     }
-    const float m = __shfl_sync(0xffffffffu, sel_v, 0);
-    const float w = lane < k ? expf(sel_v - m) : 0.f;
-    float sum = w;
 #pragma unroll
-    for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    if (lane < k) {
-      topk_idx[(size_t)t * k + lane] = sel_e;
-      gate[(size_t)t * k + lane] = w / sum;
-      atomicAdd(&hist[sel_e], 1);
+    for (int i = 0; i < ILP; ++i) {
+      const int t = t0 + i;
+      const float m = __shfl_sync(0xffffffffu, sel_v[i], 0);
+      const float w = lane < k ? expf(sel_v[i] - m) : 0.f;
+      float sum = w;
+#pragma unroll
+      for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      if (t < T && lane < k) {
+        topk_idx[(size_t)t * k + lane] = sel_e[i];
+        gate[(size_t)t * k + lane] = w / sum;
+        atomicAdd(&hist[sel_e[i]], 1);
+      }
     }
   }
   __syncthreads();
@@ -89,7 +124,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(
 }
 
 // Single block: per-expert totals and the per-(expert, block) exclusive
-// bases, then the exclusive scans over experts (logical and padded).
+// bases (one warp per expert at a time: a shuffle scan over 32 router blocks
+// per step), then the exclusive scans over experts (logical and padded).
 __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ block_hist, int nb,
                                                     int E, int32_t* __restrict__ block_base,
                                                     int32_t* __restrict__ counts,
@@ -97,21 +133,32 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
                                                     int32_t* __restrict__ padded_offsets) {
   __shared__ int s_cnt[kMaxE];
   __shared__ int s_pad[kMaxE + 1];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int b = 0; b < nb; ++b) {
-      const int c = block_hist[(size_t)e * nb + b];
-      block_base[(size_t)e * nb + b] = run;
-      run += c;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int e = warp; e < E; e += nw) {
+    const int32_t* h = block_hist + (size_t)e * nb;
+    int32_t* bb = block_base + (size_t)e * nb;
+    int carry = 0;
+    for (int b0 = 0; b0 < nb; b0 += 32) {
+      const int b = b0 + lane;
+      const int c = b < nb ? h[b] : 0;
+      int x = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+      }
+      if (b < nb) bb[b] = carry + x - c;
+      carry += __shfl_sync(0xffffffffu, x, 31);
     }
-    s_cnt[e] = run;
-    s_pad[e] = (run + kAlign - 1) / kAlign * kAlign;
-    counts[e] = run;
+    if (lane == 0) {
+      s_cnt[e] = carry;
+      s_pad[e] = (carry + kAlign - 1) / kAlign * kAlign;
+      counts[e] = carry;
+    }
   }
   __syncthreads();
   // E <= 1024: a warp-parallel scan over 32-expert chunks.
   if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
     int carry_o = 0, carry_p = 0;
     for (int c0 = 0; c0 < E; c0 += 32) {
       const int e = c0 + lane;
@@ -206,7 +253,7 @@ __global__ void __launch_bounds__(256) scatter_kernel(
 // per token; lane j < k holds slot j; the row of E logits is written once,
 // coalesced.
 template <int VPL>
-__global__ void __launch_bounds__(kRouteThreads) route_backward_kernel(
+__global__ void __launch_bounds__(kBwdThreads) route_backward_kernel(
     const int32_t* __restrict__ topk_idx, const float* __restrict__ gate,
     const float* __restrict__ dgate, int T, int E, int k, float* __restrict__ dlogits,
     int32_t* status) {
@@ -252,19 +299,19 @@ cudaError_t launch_route_backward(const int32_t* topk_idx, const float* gate, co
                                   int T, int E, int k, float* dlogits, int32_t* status,
                                   cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const int blocks = (T + (kRouteThreads / 32) - 1) / (kRouteThreads / 32);
+  const int blocks = (T + (kBwdThreads / 32) - 1) / (kBwdThreads / 32);
   const int grid = blocks < 4096 ? blocks : 4096;
   const int vpl = (E + 31) / 32;
   if (vpl <= 1)
-    route_backward_kernel<1><<<grid, kRouteThreads, 0, s>>>(topk_idx, gate, dgate, T, E, k, dlogits, status);
+    route_backward_kernel<1><<<grid, kBwdThreads, 0, s>>>(topk_idx, gate, dgate, T, E, k, dlogits, status);
   else if (vpl <= 4)
-    route_backward_kernel<4><<<grid, kRouteThreads, 0, s>>>(topk_idx, gate, dgate, T, E, k, dlogits, status);
+    route_backward_kernel<4><<<grid, kBwdThreads, 0, s>>>(topk_idx, gate, dgate, T, E, k, dlogits, status);
   else if (vpl <= 8)
-    route_backward_kernel<8><<<grid, kRouteThreads, 0, s>>>(topk_idx, gate, dgate, T, E, k, dlogits, status);
+    route_backward_kernel<8><<<grid, kBwdThreads, 0, s>>>(topk_idx, gate, dgate, T, E, k, dlogits, status);
   else if (vpl <= 16)
-    route_backward_kernel<16><<<grid, kRouteThreads, 0, s>>>(topk_idx, gate, dgate, T, E, k, dlogits, status);
+    route_backward_kernel<16><<<grid, kBwdThreads, 0, s>>>(topk_idx, gate, dgate, T, E, k, dlogits, status);
   else
-    route_backward_kernel<32><<<grid, kRouteThreads, 0, s>>>(topk_idx, gate, dgate, T, E, k, dlogits, status);
+    route_backward_kernel<32><<<grid, kBwdThreads, 0, s>>>(topk_idx, gate, dgate, T, E, k, dlogits, status);
   return cudaGetLastError();
 }
 
@@ -275,15 +322,15 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* topk
   if (nb == 0) return cudaSuccess;
   const int vpl = (E + 31) / 32;
   if (vpl <= 1)
-    route_kernel<1><<<nb, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
+    route_kernel<1><<<nb, RouteShape<1>::THREADS, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
   else if (vpl <= 4)
-    route_kernel<4><<<nb, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
+    route_kernel<4><<<nb, RouteShape<4>::THREADS, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
   else if (vpl <= 8)
-    route_kernel<8><<<nb, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
+    route_kernel<8><<<nb, RouteShape<8>::THREADS, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
   else if (vpl <= 16)
-    route_kernel<16><<<nb, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
+    route_kernel<16><<<nb, RouteShape<16>::THREADS, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
   else
-    route_kernel<32><<<nb, kRouteThreads, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
+    route_kernel<32><<<nb, RouteShape<32>::THREADS, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
   return cudaGetLastError();
 }
 

@@ -63,6 +63,40 @@ def test_small_shapes_full(cfg, mode):
 
 
 @pytest.mark.parametrize("mode", ["mxfp8", "fp8_bwd"])
+def test_small_shapes_single_cta_tiles(mode):
+    """The block-scaled GEMMs on single-CTA 128-row tiles (instead of
+    256-row tiles over an SM pair) give the same parity."""
+    import mixture_experts_layer_18_gb300 as M
+    M.moe_set_debug(M.MOE_DEBUG_SINGLE_CTA, 0)
+    try:
+        test_small_shapes_full(SMALL[1], mode)
+    finally:
+        M.moe_set_debug(0, 0)
+
+
+def test_pair_and_single_cta_agree_bitwise():
+    """Pair and single-CTA tiles run the same block-scaled MMAs over the same
+    K order, so their GEMM results are bit-identical.  d(gate) sums each
+    row's products over two column halves on pairs (two epilogue warps per
+    row) and in one pass on single CTAs, so it agrees to rounding only."""
+    import torch
+    import mixture_experts_layer_18_gb300 as M
+    cfg = SMALL[2]
+    inp = make_inputs(cfg, 4)
+    _, a = _run(cfg, inp, "mxfp8")
+    M.moe_set_debug(M.MOE_DEBUG_SINGLE_CTA, 0)
+    try:
+        _, b = _run(cfg, inp, "mxfp8")
+    finally:
+        M.moe_set_debug(0, 0)
+    for k in a:
+        if k == "dgate":
+            assert rel_err(to_f64(a[k]), to_f64(b[k])) <= 1e-6, k
+        else:
+            assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("mode", ["mxfp8", "fp8_bwd"])
 def test_full_size_235b_sampled(mode):
     """235B layer shape.  The oracle is run on k=1 sub-batches: Y, dX and
     d(gate) of a few tokens are rebuilt from one-row sub-problems of each of
