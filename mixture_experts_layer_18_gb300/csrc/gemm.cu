@@ -504,6 +504,12 @@ __device__ __forceinline__ void load32(const Elt* src, float (&v)[32]) {
   }
 }
 
+// SiLU pieces for the epilogues, with the fast reciprocal (2 ulp): the
+// results are rounded to bf16 right after, so fp32 division rounding is
+// irrelevant.  For u below about -88, exp(-u) is +inf and both give 0.
+__device__ __forceinline__ float sigmoid_f(float u) { return __fdividef(1.f, 1.f + __expf(-u)); }
+__device__ __forceinline__ float silu_f(float u) { return __fdividef(u, 1.f + __expf(-u)); }
+
 template <int NTHREADS>
 __device__ __forceinline__ void epi_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(NTHREADS) : "memory");
@@ -603,7 +609,30 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
     tc_fence_after();
     __syncwarp();
     const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * C::BN;
-    float v[32], w[32];
+    float v[32], w[32], x[64];
+    // 64 results of this thread's row: bf16 through both staging buffers and
+    // two bulk stores (3-D [E, M, N] view when z >= 0), fp32 directly
+    auto emit64 = [&](const float (&y)[64], Elt* dst, int xc, int yc, int z, bool ok) {
+      if constexpr (TS) {
+        stage_begin();
+        stage_bf16_row(sb0, lane, *reinterpret_cast<const float(*)[32]>(&y[0]));
+        stage_bf16_row(sb1, lane, *reinterpret_cast<const float(*)[32]>(&y[32]));
+        stage_end();
+        if (lane == 0) {
+          if (z >= 0) {
+            tma_store_3d(&g.tmO, sb0, xc, yc, z);
+            tma_store_3d(&g.tmO, sb1, xc + 32, yc, z);
+          } else {
+            tma_store_2d(&g.tmO, sb0, xc, yc);
+            tma_store_2d(&g.tmO, sb1, xc + 32, yc);
+          }
+          bulk_commit();
+        }
+      } else if (ok) {
+        store32<Elt>(dst, *reinterpret_cast<const float(*)[32]>(&y[0]));
+        store32<Elt>(dst + 32, *reinterpret_cast<const float(*)[32]>(&y[32]));
+      }
+    };
     if (!ti.valid) {
       // rows past the tile's expert (odd m-block count) or past M: no output
     } else if (ti.kind == GK_FWD1) {
@@ -612,8 +641,7 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       Elt* h13 = g.out2 ? static_cast<Elt*>(g.out2) + (size_t)row * g.ld_out2 + ti.n0 : nullptr;
 #pragma unroll 1
       for (int c = cb; c < cb + cw; c += 32) {
-        tmem_ld32(taddr + c, v);               // u: gate half
-        tmem_ld32(taddr + C::BN / 2 + c, w);   // v: up half
+        tmem_ld32x2(taddr + c, taddr + C::BN / 2 + c, v, w);   // u: gate half, v: up half
         if (h13) {
           if constexpr (TS) {
             stage_begin();
@@ -631,7 +659,7 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
           }
         }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = v[i] / (1.f + __expf(-v[i])) * w[i];
+        for (int i = 0; i < 32; ++i) v[i] = silu_f(v[i]) * w[i];
         if constexpr (TS) {
           stage_begin();
           stage_bf16_row(sb0, lane, v);
@@ -654,21 +682,11 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       const float gt = a >= 0 ? g.gate[a] : 0.f;
       Elt* out = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
 #pragma unroll 1
-      for (int c = cb; c < cb + cw; c += 32) {
-        tmem_ld32(taddr + c, v);
+      for (int c = cb; c < cb + cw; c += 64) {
+        tmem_ld64(taddr + c, x);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= gt;
-        if constexpr (TS) {
-          stage_begin();
-          stage_bf16_row(sb0, lane, v);
-          stage_end();
-          if (lane == 0) {
-            tma_store_2d(&g.tmO, sb0, ti.n0 + c, yrow);
-            bulk_commit();
-          }
-        } else {
-          store32<Elt>(out + c, v);
-        }
+        for (int i = 0; i < 64; ++i) x[i] *= gt;
+        emit64(x, out + c, ti.n0 + c, yrow, -1, true);
       }
     } else if (ti.kind == GK_BWD_D) {
       const int row = ti.m0 + r;
@@ -693,7 +711,7 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float u = v[i], vv = w[i];
-          const float sg = 1.f / (1.f + __expf(-u));
+          const float sg = sigmoid_f(u);
           const float si = u * sg;
           part += si * vv * D[i];
           const float dA = gt * D[i];
@@ -727,43 +745,23 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       const int row = ti.m0 + r;
       Elt* out = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
 #pragma unroll 1
-      for (int c = cb; c < cb + cw; c += 32) {
-        tmem_ld32(taddr + c, v);
-        if constexpr (TS) {
-          stage_begin();
-          stage_bf16_row(sb0, lane, v);
-          stage_end();
-          if (lane == 0) {
-            tma_store_2d(&g.tmO, sb0, ti.n0 + c, yrow);
-            bulk_commit();
-          }
-        } else {
-          store32<Elt>(out + c, v);
-        }
+      for (int c = cb; c < cb + cw; c += 64) {
+        tmem_ld64(taddr + c, x);
+        emit64(x, out + c, ti.n0 + c, yrow, -1, true);
       }
     } else {  // GK_DW
       const bool valid = ti.m0 + r < g.M;
       Elt* out = static_cast<Elt*>(g.out) + ((size_t)ti.e * g.M + ti.m0 + r) * g.ld_out + ti.n0;
 #pragma unroll 1
-      for (int c = cb; c < cb + cw; c += 32) {
+      for (int c = cb; c < cb + cw; c += 64) {
         if (ti.nk > 0) {
-          tmem_ld32(taddr + c, v);
+          tmem_ld64(taddr + c, x);
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          for (int i = 0; i < 64; ++i) x[i] = 0.f;
         }
-        if constexpr (TS) {
-          // rows past M are outside the [E, M, N] view: the store clips them
-          stage_begin();
-          stage_bf16_row(sb0, lane, v);
-          stage_end();
-          if (lane == 0) {
-            tma_store_3d(&g.tmO, sb0, ti.n0 + c, ti.m0 + q * 32, ti.e);
-            bulk_commit();
-          }
-        } else {
-          if (valid) store32<Elt>(out + c, v);
-        }
+        // rows past M are outside the [E, M, N] view: the bulk store clips them
+        emit64(x, out + c, ti.n0 + c, ti.m0 + q * 32, ti.e, valid);
       }
     }
     tc_fence_before();
