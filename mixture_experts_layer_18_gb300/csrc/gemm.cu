@@ -633,7 +633,72 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
         store32<Elt>(dst + 32, *reinterpret_cast<const float(*)[32]>(&y[32]));
       }
     };
-    if (!ti.valid) {
+    bool released = false;
+    if constexpr (C::EPI_WARPS == 8) {
+      // Block-scaled pairs hold their only accumulator until it is
+      // released: for the plain kinds the warp's 128 columns are read and
+      // packed to bf16 first, the accumulator is released, and the staging
+      // and bulk stores run while the next tile's MMAs do.
+      if (ti.kind == GK_FWD2 || ti.kind == GK_BWD_DX || ti.kind == GK_DW) {
+        const bool have = ti.valid && !(ti.kind == GK_DW && ti.nk == 0);   // CTA-uniform
+        float gt = 1.f;
+        if (ti.kind == GK_FWD2 && ti.valid) {
+          int a = g.assign_of_row[ti.m0 + r];
+          if (a >= g.n_assign) {          // corrupted map: treat as a pad row
+            report(P.status, MOE_ERR_BAD_INDEX);
+            a = -1;
+          }
+          gt = a >= 0 ? g.gate[a] : 0.f;
+        }
+        uint32_t pk[64];
+        if (have) {
+          tmem_ld64(taddr + cb, x);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(x[2 * i] * gt, x[2 * i + 1] * gt);
+          tmem_ld64_after(taddr + cb + 64, x, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[32 + i] = pack_bf16(x[2 * i] * gt, x[2 * i + 1] * gt);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) pk[i] = 0u;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(buf ? tempty_cl1 : tempty_cl0);
+        released = true;
+        if (ti.valid) {
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            stage_begin();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int rr = lane;
+              *reinterpret_cast<uint4*>(sb0 + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4)) =
+                  make_uint4(pk[32 * h2 + 4 * c + 0], pk[32 * h2 + 4 * c + 1],
+                             pk[32 * h2 + 4 * c + 2], pk[32 * h2 + 4 * c + 3]);
+              *reinterpret_cast<uint4*>(sb1 + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4)) =
+                  make_uint4(pk[32 * h2 + 16 + 4 * c + 0], pk[32 * h2 + 16 + 4 * c + 1],
+                             pk[32 * h2 + 16 + 4 * c + 2], pk[32 * h2 + 16 + 4 * c + 3]);
+            }
+            stage_end();
+            if (lane == 0) {
+              const int xc = ti.n0 + cb + 64 * h2;
+              if (ti.kind == GK_DW) {
+                tma_store_3d(&g.tmO, sb0, xc, ti.m0 + q * 32, ti.e);
+                tma_store_3d(&g.tmO, sb1, xc + 32, ti.m0 + q * 32, ti.e);
+              } else {
+                tma_store_2d(&g.tmO, sb0, xc, yrow);
+                tma_store_2d(&g.tmO, sb1, xc + 32, yrow);
+              }
+              bulk_commit();
+            }
+          }
+        }
+      }
+    }
+    if (released) {
+      // stored above, accumulator already released
+    } else if (!ti.valid) {
       // rows past the tile's expert (odd m-block count) or past M: no output
     } else if (ti.kind == GK_FWD1) {
       const int row = ti.m0 + r;
@@ -764,11 +829,13 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
         emit64(x, out + c, ti.n0 + c, ti.m0 + q * 32, ti.e, valid);
       }
     }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) {
-      if constexpr (C::PAIR == 2) mbar_arrive_cluster(buf ? tempty_cl1 : tempty_cl0);
-      else mbar_arrive(&tempty[buf]);
+    if (!released) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (C::PAIR == 2) mbar_arrive_cluster(buf ? tempty_cl1 : tempty_cl0);
+        else mbar_arrive(&tempty[buf]);
+      }
     }
     if (g.signal && ti.valid) {
       // Publish this tile's rows to TMA readers in other CTAs: the bulk
