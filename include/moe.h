@@ -103,11 +103,24 @@ typedef struct {
 /* Byte offsets of the tensors inside the `saved` buffer written by
  * moe_forward and read by moe_backward (rows = moe_max_rows(dims), elem =
  * 4 bytes for MOE_F32, else 2):
- *   x_perm [rows, H]   gathered tokens, expert-major, zero pad rows
+ *   x_perm [rows, H]   gathered tokens, expert-major, zero pad rows (not
+ *                      written in MOE_MXFP8 mode: the dispatch gather goes
+ *                      straight into its MXFP8 encodings, x_col below)
  *   h13    [rows, 2I]  X_perm_e W13_e before the activation (if save_for_backward)
- *   act    [rows, I]   A = silu(h13[:, :I]) * h13[:, I:]                  */
+ *   act    [rows, I]   A = silu(h13[:, :I]) * h13[:, I:]
+ * MOE_MXFP8 only (zero-sized in the other modes): the backward's MXFP8
+ * operands, which the forward quantises in the same passes as its own
+ * (E4M3 codes *_q, tensor-core scale atoms *_sf; written only with
+ * save_for_backward):
+ *   x_col   X_perm, 32-row blocks per expert group       (dW13 operand)
+ *   act_col A, 32-row blocks per expert group             (dW2 operand)
+ *   w13_row W13 [E*H, 2I], 32-column blocks along 2I      (dX operand)
+ *   w2_row  W2 [E*I, H], 32-column blocks along H          (D operand)    */
 typedef struct {
-  size_t x_perm, h13, act, total;
+  size_t x_perm, h13, act;
+  size_t x_col_q, x_col_sf, act_col_q, act_col_sf;
+  size_t w13_row_q, w13_row_sf, w2_row_q, w2_row_sf;
+  size_t total;
 } moe_saved_layout;
 
 enum { MOE_WS_ROUTE = 0, MOE_WS_FORWARD = 1, MOE_WS_BACKWARD = 2 };
@@ -219,6 +232,26 @@ moe_status moe_quantize_mxfp8(const void* src, int R, int C, int ld, int axis,
                               const int32_t* group_offsets, int G, uint8_t* q,
                               uint8_t* scales, int32_t* dev_status,
                               void* stream);
+
+/* Both MXFP8 encodings of one bf16 tensor from a single read (the rule of
+ * moe_quantize_mxfp8), with the scales in the tensor-core atom layout that
+ * the layer's block-scaled GEMMs read: 512-byte atoms of 128 MN indices x 128
+ * K elements, the scale of MN index mn and 32-element K block kb at byte
+ *   ((mn / 128) * kgroups + kb / 4) * 512 + (mn % 32) * 16 + ((mn / 32) % 4) * 4 + kb % 4.
+ *   q_row, s_row  blocks of 32 along each row: MN = row, kgroups = C / 128;
+ *                 s_row holds ceil(R / 128) * 128 * C / 32 bytes.
+ *   q_col, s_col  blocks of 32 rows down each column: MN = column,
+ *                 kgroups = ceil(R / 128); s_col holds C * ceil(R / 128) * 4 bytes.
+ *   q_row, q_col  uint8 [R, C] E4M3 codes (device).
+ *   src           bf16 [R, ld] (device).
+ *   rows_limit    optional device int32 (NULL: R): rows at or past it are
+ *                 neither read nor written (it must be a multiple of 32).
+ * R must be a multiple of 32, C of 128, ld >= C a multiple of 8; other sizes
+ * return MOE_ERR_INVALID_ARG. */
+moe_status moe_quantize_mxfp8_dual(const void* src, int R, int C, int ld,
+                                   const int32_t* rows_limit, uint8_t* q_row,
+                                   uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                                   int32_t* dev_status, void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* moe_status_string(moe_status s);

@@ -20,7 +20,7 @@ __all__ = [
     "MOE_DEBUG_NEVER_READY", "MOE_DEBUG_SINGLE_CTA", "MOE_DEBUG_SPLIT_BACKWARD", "moe_dims", "moe_route_out", "moe_saved_layout",
     "lib", "header_functions", "moe_max_rows", "moe_workspace_size",
     "moe_saved_layout_of", "moe_route", "moe_route_noalloc", "moe_route_backward", "moe_forward", "moe_backward",
-    "moe_quantize_mxfp8", "moe_status_string", "moe_set_debug", "moe_set_gemm_events",
+    "moe_quantize_mxfp8", "moe_quantize_mxfp8_dual", "moe_status_string", "moe_set_debug", "moe_set_gemm_events",
     "MoEError",
 ]
 
@@ -49,7 +49,10 @@ class moe_route_out(ctypes.Structure):
 
 
 class moe_saved_layout(ctypes.Structure):
-    _fields_ = [("x_perm", _c_size), ("h13", _c_size), ("act", _c_size), ("total", _c_size)]
+    _fields_ = [("x_perm", _c_size), ("h13", _c_size), ("act", _c_size),
+                ("x_col_q", _c_size), ("x_col_sf", _c_size), ("act_col_q", _c_size),
+                ("act_col_sf", _c_size), ("w13_row_q", _c_size), ("w13_row_sf", _c_size),
+                ("w2_row_q", _c_size), ("w2_row_sf", _c_size), ("total", _c_size)]
 
 
 class MoEError(RuntimeError):
@@ -72,6 +75,8 @@ _SIGS = {
                               _c_size, _vp, _vp]),
     "moe_quantize_mxfp8": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp,
                                     _vp, _vp]),
+    "moe_quantize_mxfp8_dual": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp, _vp,
+                                         _vp, _vp]),
     "moe_status_string": (ctypes.c_char_p, [_c_int]),
     "moe_set_debug": (None, [_c_int, _i64]),
     "moe_set_gemm_events": (None, [_c_int, _vp, _vp]),
@@ -148,6 +153,12 @@ def moe_quantize_mxfp8(src, R, C, ld, axis, group_offsets, G, q, scales, dev_sta
                        stream) -> int:
     return lib().moe_quantize_mxfp8(src, R, C, ld, axis, group_offsets, G, q, scales, dev_status,
                                     stream)
+
+
+def moe_quantize_mxfp8_dual(src, R, C, ld, rows_limit, q_row, s_row, q_col, s_col, dev_status,
+                            stream) -> int:
+    return lib().moe_quantize_mxfp8_dual(src, R, C, ld, rows_limit, q_row, s_row, q_col, s_col,
+                                         dev_status, stream)
 
 
 def moe_status_string(code: int) -> str:

@@ -54,6 +54,20 @@ cudaError_t launch_dgate_reduce(const float* partial, int nt, int n_assign,
 cudaError_t launch_quantize(const void* src, int R, int C, int ld, int axis,
                             const int32_t* group_offsets, int G, uint8_t* q, uint8_t* scales,
                             int32_t* status, cudaStream_t s, int layout = 0);
+// Both layout-1 quantisations (row-wise into qr/sr, column-wise into qc/sc;
+// qc == nullptr skips the latter) from one read; R % 32 == 0, C % 128 == 0;
+// rows >= *rows_dev (if given) untouched.  With `gather`, output row r is
+// token row assign_of_row[r] / k of src (pad rows 0), and with gather->gate
+// the column-wise encoding is taken of bf16(gate[a] * row).
+struct DualGather {
+  const int32_t* assign_of_row;
+  int k, n_assign;
+  const float* gate;     // optional
+  int32_t* status;
+};
+cudaError_t launch_quantize_dual(const void* src, int R, int C, int ld, const int32_t* rows_dev,
+                                 uint8_t* qr, uint8_t* sr, uint8_t* qc, uint8_t* sc,
+                                 cudaStream_t s, const DualGather* gather = nullptr);
 
 // gemm.cu
 struct GemmDesc {

@@ -158,13 +158,15 @@ BwdWs bwd_ws(const moe_dims* d) {
     const size_t rp = (size_t)rows_pad(d), EH = (size_t)d->E * d->H, EI = (size_t)d->E * d->I;
     const size_t H = d->H, I = d->I;
     w.dy = mx_carve(o, rows, rp, H);
-    w.w2r = mx_carve(o, EI, EI, H);
-    w.actc = mx_carve(o, rows, rp, I);
     w.dygc = mx_carve(o, rows, rp, H);
     w.dh13r = mx_carve(o, rows, rp, 2 * I);
     w.dh13c = mx_carve(o, rows, rp, 2 * I);
-    w.w13r = mx_carve(o, EH, EH, 2 * I);
-    w.xpc = mx_carve(o, rows, rp, H);
+    if (d->mode != MOE_MXFP8) {   // mxfp8: the forward leaves these in `saved`
+      w.w2r = mx_carve(o, EI, EI, H);
+      w.actc = mx_carve(o, rows, rp, I);
+      w.w13r = mx_carve(o, EH, EH, 2 * I);
+      w.xpc = mx_carve(o, rows, rp, H);
+    }
   }
   w.total = o;
   return w;
@@ -186,11 +188,21 @@ RouteWs route_ws(const moe_dims* d) {
 
 moe_saved_layout saved_layout(const moe_dims* d) {
   moe_saved_layout s;
+  memset(&s, 0, sizeof(s));
   const size_t rows = (size_t)max_rows(d), es = elem_bytes(d);
   size_t o = 0;
   s.x_perm = o; o += align256(rows * d->H * es);
   s.h13 = o; o += align256(rows * 2 * d->I * es);
   s.act = o; o += align256(rows * d->I * es);
+  if (d->mode == MOE_MXFP8) {
+    const size_t rp = (size_t)rows_pad(d), EH = (size_t)d->E * d->H, EI = (size_t)d->E * d->I;
+    const MxBuf x = mx_carve(o, rows, rp, d->H), a = mx_carve(o, rows, rp, d->I);
+    const MxBuf w13 = mx_carve(o, EH, EH, 2 * (size_t)d->I), w2 = mx_carve(o, EI, EI, d->H);
+    s.x_col_q = x.q; s.x_col_sf = x.sf;
+    s.act_col_q = a.q; s.act_col_sf = a.sf;
+    s.w13_row_q = w13.q; s.w13_row_sf = w13.sf;
+    s.w2_row_q = w2.q; s.w2_row_sf = w2.sf;
+  }
   s.total = o;
   return s;
 }
@@ -235,15 +247,47 @@ cudaError_t quant_cols(const void* src, int64_t R, int C, const int32_t* go, int
                        int32_t* st, cudaStream_t s) {
   return launch_quantize(src, (int)R, C, C, 0, go, G, (uint8_t*)m.q, (uint8_t*)m.sf, st, s, 1);
 }
+// row-wise into `rw` and column-wise into `cw` (if given) from one read;
+// rows at or past *rows_dev (if given) untouched; with `g`, rows are gathered
+// token rows of src (see DualGather)
+cudaError_t quant_both(const void* src, int64_t R, int C, const int32_t* rows_dev, const Mx& rw,
+                       const Mx* cw, cudaStream_t s, const DualGather* g = nullptr) {
+  return launch_quantize_dual(src, (int)R, C, C, rows_dev, (uint8_t*)rw.q, (uint8_t*)rw.sf,
+                              cw ? (uint8_t*)cw->q : nullptr, cw ? (uint8_t*)cw->sf : nullptr, s, g);
+}
+// the backward's operands that the mxfp8 forward writes into `saved`
+struct MxSaved {
+  Mx x_col, act_col, w13_row, w2_row;
+};
+MxSaved mx_saved(const moe_dims* d, const moe_saved_layout& sl, char* sv) {
+  const int64_t rp = rows_pad(d), EH = (int64_t)d->E * d->H, EI = (int64_t)d->E * d->I;
+  auto at = [&](size_t q, size_t sf, int64_t sf_bytes) {
+    return Mx{sv + q, reinterpret_cast<const uint8_t*>(sv + sf), sf_bytes};
+  };
+  return MxSaved{at(sl.x_col_q, sl.x_col_sf, rp * d->H / 32), at(sl.act_col_q, sl.act_col_sf, rp * d->I / 32),
+                 at(sl.w13_row_q, sl.w13_row_sf, EH * 2 * d->I / 32),
+                 at(sl.w2_row_q, sl.w2_row_sf, EI * d->H / 32)};
+}
 
-moe_status forward_mx(const moe_dims* d, const void* W13, const void* W2, const moe_route_out* r,
-                      void* x_perm, void* h13, void* act, void* zg, char* wsb, const FwdWs& w,
-                      int32_t* dev_status, cudaStream_t s) {
+// With save_for_backward, each quantisation pass also writes the backward's
+// encoding of the same tensor into `saved` (one read, both layouts).
+// The dispatch gather is fused into the first quantisation: X_perm exists
+// only as its MXFP8 encodings (saved x_perm is not written in this mode).
+moe_status forward_mx(const moe_dims* d, const void* X, const void* W13, const void* W2,
+                      const moe_route_out* r, void* h13, void* act, void* zg, char* wsb,
+                      const FwdWs& w, const MxSaved& sv, int32_t* dev_status, cudaStream_t s) {
   const int64_t rows = max_rows(d), rp = rows_pad(d);
   const int H = d->H, I = d->I, E = d->E;
   const Mx x = mx_at(wsb, w.x), w13 = mx_at(wsb, w.w13), a = mx_at(wsb, w.a), w2 = mx_at(wsb, w.w2);
-  MOE_TRY(quant_rows(x_perm, rows, H, x, dev_status, s));
-  MOE_TRY(quant_cols(W13, (int64_t)E * H, 2 * I, nullptr, 0, w13, dev_status, s));
+  const int32_t* tpad = r->padded_offsets + E;
+  const bool both = d->save_for_backward != 0;
+  const DualGather gx{r->assign_of_row, d->top_k, d->T * d->top_k, nullptr, dev_status};
+  MOE_TRY(quant_both(X, rows, H, tpad, x, both ? &sv.x_col : nullptr, s, &gx));
+  if (both) {
+    MOE_TRY(quant_both(W13, (int64_t)E * H, 2 * I, nullptr, sv.w13_row, &w13, s));
+  } else {
+    MOE_TRY(quant_cols(W13, (int64_t)E * H, 2 * I, nullptr, 0, w13, dev_status, s));
+  }
   moe_status st;
   EngineLaunch L;
   memset(&L, 0, sizeof(L));
@@ -269,8 +313,13 @@ moe_status forward_mx(const moe_dims* d, const void* W13, const void* W2, const 
     MOE_TRY(launch_engine(L, s, &st));
     if (st != MOE_OK) return st;
   }
-  MOE_TRY(quant_rows(act, rows, I, a, dev_status, s));
-  MOE_TRY(quant_cols(W2, (int64_t)E * I, H, nullptr, 0, w2, dev_status, s));
+  if (both) {
+    MOE_TRY(quant_both(act, rows, I, tpad, a, &sv.act_col, s));
+    MOE_TRY(quant_both(W2, (int64_t)E * I, H, nullptr, sv.w2_row, &w2, s));
+  } else {
+    MOE_TRY(quant_rows(act, rows, I, a, dev_status, s));
+    MOE_TRY(quant_cols(W2, (int64_t)E * I, H, nullptr, 0, w2, dev_status, s));
+  }
   {
     GemmDesc& g = L.prob[0];
     g = GemmDesc{};
@@ -292,22 +341,32 @@ moe_status forward_mx(const moe_dims* d, const void* W13, const void* W2, const 
 // Backward with MXFP8 GEMMs (modes mxfp8 and fp8_bwd).  dh13 must be
 // quantised before dX and dW13 can read it, so the gradient GEMMs run as
 // two launches: {D + dSwiGLU, dW2}, then {dX, dW13}.
-moe_status backward_mx(const moe_dims* d, const void* W13, const void* W2,
+// The dY gather is fused into its quantisation: dY_perm and gate * dY_perm
+// exist only as their MXFP8 encodings.
+moe_status backward_mx(const moe_dims* d, const void* dY, const void* W13, const void* W2,
                        const moe_route_out* r, const void* x_perm, const void* h13,
-                       const void* act, void* dy_perm, void* dyg_perm, void* dh13, void* dxp,
+                       const void* act, void* dh13, void* dxp,
                        float* partial, void* dW13, void* dW2, char* wsb, const BwdWs& w,
-                       int32_t* dev_status, cudaStream_t s) {
+                       const MxSaved& sv, int32_t* dev_status, cudaStream_t s) {
   const int64_t rows = max_rows(d), rp = rows_pad(d);
   const int H = d->H, I = d->I, E = d->E;
   const int kgt = (int)(rp / 128);   // K groups of the token axis
-  const Mx dy = mx_at(wsb, w.dy), w2r = mx_at(wsb, w.w2r), actc = mx_at(wsb, w.actc),
-           dygc = mx_at(wsb, w.dygc), dh13r = mx_at(wsb, w.dh13r), dh13c = mx_at(wsb, w.dh13c),
-           w13r = mx_at(wsb, w.w13r), xpc = mx_at(wsb, w.xpc);
+  // mxfp8: X_perm, A, W13 and W2 were quantised for the backward by the
+  // forward (saved); fp8_bwd (bf16 forward): quantised here
+  const bool saved_mx = d->mode == MOE_MXFP8;
+  const Mx dy = mx_at(wsb, w.dy), dygc = mx_at(wsb, w.dygc), dh13r = mx_at(wsb, w.dh13r),
+           dh13c = mx_at(wsb, w.dh13c);
+  const Mx w2r = saved_mx ? sv.w2_row : mx_at(wsb, w.w2r);
+  const Mx actc = saved_mx ? sv.act_col : mx_at(wsb, w.actc);
+  const Mx w13r = saved_mx ? sv.w13_row : mx_at(wsb, w.w13r);
+  const Mx xpc = saved_mx ? sv.x_col : mx_at(wsb, w.xpc);
   const int32_t* po = r->padded_offsets;
-  MOE_TRY(quant_rows(dy_perm, rows, H, dy, dev_status, s));
-  MOE_TRY(quant_rows(W2, (int64_t)E * I, H, w2r, dev_status, s));
-  MOE_TRY(quant_cols(act, rows, I, po, E, actc, dev_status, s));
-  MOE_TRY(quant_cols(dyg_perm, rows, H, po, E, dygc, dev_status, s));
+  const DualGather gy{r->assign_of_row, d->top_k, d->T * d->top_k, r->gate, dev_status};
+  MOE_TRY(quant_both(dY, rows, H, po + E, dy, &dygc, s, &gy));
+  if (!saved_mx) {
+    MOE_TRY(quant_rows(W2, (int64_t)E * I, H, w2r, dev_status, s));
+    MOE_TRY(quant_cols(act, rows, I, po, E, actc, dev_status, s));
+  }
   EngineLaunch L;
   memset(&L, 0, sizeof(L));
   L.E = E;
@@ -342,10 +401,11 @@ moe_status backward_mx(const moe_dims* d, const void* W13, const void* W2,
     MOE_TRY(launch_engine(L, s, &st));
     if (st != MOE_OK) return st;
   }
-  MOE_TRY(quant_rows(dh13, rows, 2 * I, dh13r, dev_status, s));
-  MOE_TRY(quant_cols(dh13, rows, 2 * I, po, E, dh13c, dev_status, s));
-  MOE_TRY(quant_rows(W13, (int64_t)E * H, 2 * I, w13r, dev_status, s));
-  MOE_TRY(quant_cols(x_perm, rows, H, po, E, xpc, dev_status, s));
+  MOE_TRY(quant_both(dh13, rows, 2 * I, po + E, dh13r, &dh13c, s));
+  if (!saved_mx) {
+    MOE_TRY(quant_rows(W13, (int64_t)E * H, 2 * I, w13r, dev_status, s));
+    MOE_TRY(quant_cols(x_perm, rows, H, po, E, xpc, dev_status, s));
+  }
   {
     L.nprob = 2;
     GemmDesc& gx = L.prob[0];
@@ -466,11 +526,9 @@ moe_status moe_forward(const moe_dims* d, const void* X, const void* W13, const 
   void* zg = static_cast<char*>(ws) + w.zg;
 
   if (mx_fwd(d)) {
-    MOE_TRY(launch_gather_rows(X, x_perm, d->H, es, d->top_k, n_assign, r->assign_of_row,
-                               r->padded_offsets, d->E, rows, dev_status, s));
     EventScope timing(MOE_WS_FORWARD, s);
-    const moe_status st = forward_mx(d, W13, W2, r, x_perm, h13, act, zg, static_cast<char*>(ws),
-                                     w, dev_status, s);
+    const moe_status st = forward_mx(d, X, W13, W2, r, h13, act, zg, static_cast<char*>(ws), w,
+                                     mx_saved(d, sl, sv), dev_status, s);
     if (st != MOE_OK) return st;
     timing.finish();
     MOE_TRY(launch_combine(zg, Y, d->T, d->H, es, d->top_k, r->row_of_assign, rows, dev_status, s));
@@ -575,15 +633,11 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
   float* partial = reinterpret_cast<float*>(wb + w.partial);
   int32_t* ready = reinterpret_cast<int32_t*>(wb + w.ready);
 
-  MOE_TRY(launch_gather_grad(dY, dy_perm, dyg_perm, d->H, es, d->top_k, n_assign,
-                             r->assign_of_row, r->gate, r->padded_offsets, d->E, rows, dev_status,
-                             s));
-  MOE_TRY(cudaMemsetAsync(ready, 0, ((rows + 127) / 128 + 1) * sizeof(int32_t), s));
-
   if (mx_bwd(d)) {
     EventScope timing(MOE_WS_BACKWARD, s);
-    const moe_status st = backward_mx(d, W13, W2, r, x_perm, h13, act, dy_perm, dyg_perm, dh13, dxp,
-                                      partial, dW13, dW2, wb, w, dev_status, s);
+    const moe_status st = backward_mx(d, dY, W13, W2, r, x_perm, h13, act, dh13, dxp,
+                                      partial, dW13, dW2, wb, w,
+                                      mx_saved(d, sl, const_cast<char*>(sv)), dev_status, s);
     if (st != MOE_OK) return st;
     timing.finish();
     MOE_TRY(launch_combine(dxp, dX, d->T, d->H, es, d->top_k, r->row_of_assign, rows, dev_status,
@@ -592,6 +646,10 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
                                 dev_status, s));
     return MOE_OK;
   }
+  MOE_TRY(launch_gather_grad(dY, dy_perm, dyg_perm, d->H, es, d->top_k, n_assign,
+                             r->assign_of_row, r->gate, r->padded_offsets, d->E, rows, dev_status,
+                             s));
+  MOE_TRY(cudaMemsetAsync(ready, 0, ((rows + 127) / 128 + 1) * sizeof(int32_t), s));
   const bool f32 = d->mode == MOE_F32;
   const int64_t lt = ld_t(d);
   float* act_t = reinterpret_cast<float*>(wb + w.act_t);
@@ -698,6 +756,20 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
   MOE_TRY(launch_combine(dxp, dX, d->T, d->H, es, d->top_k, r->row_of_assign, rows, dev_status, s));
   MOE_TRY(launch_dgate_reduce(partial, w.nt_d, n_assign, r->row_of_assign, rows, dgate, dev_status,
                               s));
+  return MOE_OK;
+}
+
+moe_status moe_quantize_mxfp8_dual(const void* src, int R, int C, int ld,
+                                   const int32_t* rows_limit, uint8_t* q_row, uint8_t* s_row,
+                                   uint8_t* q_col, uint8_t* s_col, int32_t* dev_status,
+                                   void* stream) {
+  if (R < 0 || C <= 0 || R % 32 || C % 128 || ld < C || ld % 8 || !aligned16(dev_status))
+    return MOE_ERR_INVALID_ARG;
+  if (R == 0) return MOE_OK;
+  if (!aligned16(src) || !aligned16(q_row) || !aligned16(q_col) || !s_row || !s_col)
+    return MOE_ERR_INVALID_ARG;
+  MOE_TRY(launch_quantize_dual(src, R, C, ld, rows_limit, q_row, s_row, q_col, s_col,
+                               static_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 

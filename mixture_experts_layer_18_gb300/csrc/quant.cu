@@ -150,6 +150,156 @@ __global__ void __launch_bounds__(256) quant_colwise_kernel(const __nv_bfloat16*
   }
 }
 
+// Both quantisations of one bf16 tensor from a single read, tensor-core
+// scale layout: row-wise (blocks of 32 along each row; MN = rows, K = the
+// C columns) and column-wise (blocks of 32 rows down each column; MN =
+// columns, K = rows, kgroups = ceil(R / 128)).  A block of 256 threads
+// stages a 64-row x 128-column tile (two 32-row blocks) in shared memory,
+// finds its 256 column-block maxima (one per thread) and its row-block
+// maxima (pairs of threads, one shuffle), then every thread encodes 16
+// consecutive elements of a row twice and writes each set of 16 codes with
+// one 16-byte store (eight threads cover a row: coalesced); the next tile's
+// loads are issued before this one is encoded.  Codes and scale bytes are those of the
+// two kernels above.  Rows at or past `rows` (a device value, e.g. the
+// padded row total) are neither read nor written; they start on a 32-row
+// boundary.  qc == nullptr skips the column-wise output.
+// SRC: 0 = row r of src; 1 = token row assign_of_row[r] / k of src (the
+// dispatch gather; pad rows read as 0); 2 = the same gather, with the
+// column-wise encoding taken of gate[a] * row rounded to bf16 (the
+// gate-scaled gradient rows of the weight-gradient GEMM).
+template <int SRC>
+__global__ void __launch_bounds__(256, 4) quant_dual_kernel(
+    const __nv_bfloat16* __restrict__ src, int R, int C, int ld, const int32_t* __restrict__ rows_dev,
+    const int32_t* __restrict__ assign_of_row, int k, int n_assign, const float* __restrict__ gate,
+    int32_t* status, uint8_t* __restrict__ qr, uint8_t* __restrict__ sr, uint8_t* __restrict__ qc,
+    uint8_t* __restrict__ sc) {
+  constexpr int TR = 64;                             // tile rows (two 32-row blocks)
+  constexpr int PITCH = 68;                          // words per tile row (272 B)
+  __shared__ __align__(16) uint32_t tile[TR][PITCH];                  // TR rows x 128 bf16
+  __shared__ __align__(16) uint32_t tileg[SRC == 2 ? TR : 1][PITCH];  // bf16(gate * row)
+  __shared__ float s_cinv[2][128];                   // column-wise 2^-s per (row block, column)
+  const int rows = rows_dev ? min(*rows_dev, R) : R;
+  const int nct = C / 128, nrt = (rows + TR - 1) / TR;
+  const int64_t ntiles = (int64_t)nrt * nct;
+  const int64_t kg_rows = (R + 127) / 128;
+  // this thread's four 16-byte chunks of a tile (and, gathered, their gate)
+  uint4 v[4];
+  float gv[4];
+  auto fetch = [&](int64_t t) {
+    const int rt = (int)(t / nct), ct = (int)(t - (int64_t)rt * nct);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int ch = threadIdx.x + 256 * i;
+      const int r = rt * TR + (ch >> 4), c = ch & 15;
+      v[i] = make_uint4(0, 0, 0, 0);
+      gv[i] = 0.f;
+      if (r < rows) {
+        if constexpr (SRC == 0) {
+          v[i] = __ldg(reinterpret_cast<const uint4*>(src + (size_t)r * ld + ct * 128) + c);
+        } else {
+          const int a = assign_of_row[r];
+          const bool ok = a >= 0 && a < n_assign;
+          if (a >= n_assign && c == 0) report(status, MOE_ERR_BAD_INDEX);
+          if (ok) {
+            v[i] = __ldg(reinterpret_cast<const uint4*>(src + (size_t)(a / k) * ld + ct * 128) + c);
+            if constexpr (SRC == 2) gv[i] = gate[a];
+          }
+        }
+      }
+    }
+  };
+  int64_t t = blockIdx.x;
+  if (t < ntiles) fetch(t);
+  for (; t < ntiles; t += gridDim.x) {
+    const int rt = (int)(t / nct), ct = (int)(t - (int64_t)rt * nct);
+    const int r0 = rt * TR, c0 = ct * 128;
+    const int nrb = min(TR, rows - r0) / 32;        // 32-row blocks of this tile (1 or 2)
+    __syncthreads();   // previous tile fully consumed
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int ch = threadIdx.x + 256 * i;
+      const int r = ch >> 4, c = ch & 15;
+      *reinterpret_cast<uint4*>(&tile[r][4 * c]) = v[i];
+      if constexpr (SRC == 2) {
+        const float g = gv[i];
+        *reinterpret_cast<uint4*>(&tileg[r][4 * c]) =
+            make_uint4(pack_bf16(g * bf16_lo(v[i].x), g * bf16_hi(v[i].x)),
+                       pack_bf16(g * bf16_lo(v[i].y), g * bf16_hi(v[i].y)),
+                       pack_bf16(g * bf16_lo(v[i].z), g * bf16_hi(v[i].z)),
+                       pack_bf16(g * bf16_lo(v[i].w), g * bf16_hi(v[i].w)));
+      }
+    }
+    __syncthreads();
+    if (t + gridDim.x < ntiles) fetch(t + gridDim.x);   // next tile's loads overlap this one
+    const uint32_t (*ctile)[PITCH] = SRC == 2 ? tileg : tile;   // column-wise source
+    // column maxima: thread = (row block, column)
+    if (qc) {
+      const int rb = threadIdx.x >> 7, c = threadIdx.x & 127;
+      if (rb < nrb) {
+        float am = 0.f;
+#pragma unroll 8
+        for (int r = 0; r < 32; ++r) {
+          const uint32_t w = ctile[32 * rb + r][c >> 1];
+          am = fmaxf(am, fabsf((c & 1) ? bf16_hi(w) : bf16_lo(w)));
+        }
+        const int sb = mx_scale_byte(am);
+        s_cinv[rb][c] = mx_inv_scale(sb);
+        sc[mma_scale_index(c0 + c, (r0 >> 5) + rb, kg_rows)] = (uint8_t)sb;
+      }
+    }
+    // row-wise: thread = (row, 16-column group); it and its neighbour
+    // (group ^ 1) form one 32-column block
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      const int er = (threadIdx.x >> 3) + 32 * p, eg = threadIdx.x & 7;
+      if (er >= 32 * nrb) break;
+      uint32_t w[8];
+      const uint4 v0 = *reinterpret_cast<const uint4*>(&tile[er][8 * eg]);
+      const uint4 v1 = *reinterpret_cast<const uint4*>(&tile[er][8 * eg + 4]);
+      w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+      w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+      float am = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) am = fmaxf(am, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+      const int sb = mx_scale_byte(am);
+      const float inv = mx_inv_scale(sb);
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t p0 = e4m3x2(bf16_lo(w[2 * i]) * inv, bf16_hi(w[2 * i]) * inv);
+        const uint32_t p1 = e4m3x2(bf16_lo(w[2 * i + 1]) * inv, bf16_hi(w[2 * i + 1]) * inv);
+        o[i] = p0 | (p1 << 16);
+      }
+      *reinterpret_cast<uint4*>(qr + (size_t)(r0 + er) * C + c0 + 16 * eg) =
+          make_uint4(o[0], o[1], o[2], o[3]);
+      if ((eg & 1) == 0) sr[mma_scale_index(r0 + er, (c0 >> 5) + (eg >> 1), nct)] = (uint8_t)sb;
+    }
+    if (qc) {
+      __syncthreads();   // column scales ready
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        const int er = (threadIdx.x >> 3) + 32 * p, eg = threadIdx.x & 7;
+        if (er >= 32 * nrb) break;
+        uint32_t w[8];
+        const uint4 v0 = *reinterpret_cast<const uint4*>(&ctile[er][8 * eg]);
+        const uint4 v1 = *reinterpret_cast<const uint4*>(&ctile[er][8 * eg + 4]);
+        w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+        w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float* ci = &s_cinv[p][16 * eg + 4 * i];
+          o[i] = (uint32_t)e4m3x2(bf16_lo(w[2 * i]) * ci[0], bf16_hi(w[2 * i]) * ci[1]) |
+                 ((uint32_t)e4m3x2(bf16_lo(w[2 * i + 1]) * ci[2], bf16_hi(w[2 * i + 1]) * ci[3]) << 16);
+        }
+        *reinterpret_cast<uint4*>(qc + (size_t)(r0 + er) * C + c0 + 16 * eg) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
+}
+
 int grid_cap() {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
@@ -180,6 +330,28 @@ cudaError_t launch_quantize(const void* src, int R, int C, int ld, int axis,
   else
     quant_colwise_kernel<0><<<(int)blocks, 256, 0, s>>>(x, R, C, ld, group_offsets, G, q, scales,
                                                         status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_dual(const void* src, int R, int C, int ld, const int32_t* rows_dev,
+                                 uint8_t* qr, uint8_t* sr, uint8_t* qc, uint8_t* sc,
+                                 cudaStream_t s, const DualGather* gather) {
+  const int64_t tiles = (int64_t)((R + 63) / 64) * (C / 128);
+  if (tiles == 0) return cudaSuccess;
+  const int cap = grid_cap();
+  const int blocks = (int)(tiles < cap ? tiles : cap);
+  const __nv_bfloat16* x = (const __nv_bfloat16*)src;
+  if (!gather)
+    quant_dual_kernel<0><<<blocks, 256, 0, s>>>(x, R, C, ld, rows_dev, nullptr, 1, 0, nullptr,
+                                                nullptr, qr, sr, qc, sc);
+  else if (!gather->gate)
+    quant_dual_kernel<1><<<blocks, 256, 0, s>>>(x, R, C, ld, rows_dev, gather->assign_of_row,
+                                                gather->k, gather->n_assign, nullptr,
+                                                gather->status, qr, sr, qc, sc);
+  else
+    quant_dual_kernel<2><<<blocks, 256, 0, s>>>(x, R, C, ld, rows_dev, gather->assign_of_row,
+                                                gather->k, gather->n_assign, gather->gate,
+                                                gather->status, qr, sr, qc, sc);
   return cudaGetLastError();
 }
 

@@ -106,3 +106,58 @@ def test_golden_blocks_on_gpu():
         assert int(sc[i, 0]) == case["scale"], case["name"]
         want = [int(c, 16) for c in case["codes"]]
         assert list(q[i, : len(want)]) == want, case["name"]
+
+
+def _atom_byte(mn, kb, kgroups):
+    """Byte of (MN index, 32-element K block) in the tensor-core scale atoms
+    (512-byte atoms of 128 MN indices x 4 K blocks), as declared in moe.h."""
+    mn = np.asarray(mn)
+    kb = np.asarray(kb)
+    return ((mn // 128) * kgroups + kb // 4) * 512 + (mn % 32) * 16 + ((mn // 32) % 4) * 4 + kb % 4
+
+
+def _dual(bits, rows_limit=None):
+    import torch
+    R, C = bits.shape
+    src = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda()
+    Rp = (R + 127) // 128 * 128
+    qr = torch.full((R, C), 0xAB, dtype=torch.uint8, device="cuda")
+    qc = torch.full((R, C), 0xAB, dtype=torch.uint8, device="cuda")
+    sr = torch.full((Rp * C // 32,), 0xCD, dtype=torch.uint8, device="cuda")
+    sc = torch.full((Rp * C // 32,), 0xCD, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    lim = torch.tensor([rows_limit], dtype=torch.int32, device="cuda") if rows_limit is not None else None
+    rc = M.moe_quantize_mxfp8_dual(src.data_ptr(), R, C, C, lim.data_ptr() if lim is not None else None,
+                                   qr.data_ptr(), sr.data_ptr(), qc.data_ptr(), sc.data_ptr(),
+                                   status.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == M.MOE_OK
+    torch.cuda.synchronize()
+    assert int(status[0].item()) == 0
+    return qr.cpu().numpy(), sr.cpu().numpy(), qc.cpu().numpy(), sc.cpu().numpy()
+
+
+@pytest.mark.parametrize("R,C", [(32, 128), (256, 384), (96, 256), (1024, 1024)])
+def test_dual_bit_exact(R, C):
+    """Row-wise and column-wise encodings from the one-read kernel equal the
+    oracle's, codes and scale bytes (unpacked from the atom layout)."""
+    bits = _draw(R, C, 5 * R + C)
+    x = bf16_bits_to_f32(bits)
+    qr, sr, qc, sc = _dual(bits)
+    rq, rs = O.quantize_mxfp8(x, 1)          # [R, C], [R, C/32]
+    cq, cs = O.quantize_mxfp8(x, 0)          # [R, C], [R/32, C]
+    assert np.array_equal(qr, rq)
+    assert np.array_equal(qc, cq)
+    r, kb = np.meshgrid(np.arange(R), np.arange(C // 32), indexing="ij")
+    assert np.array_equal(sr[_atom_byte(r, kb, C // 128)], rs)
+    rb, c = np.meshgrid(np.arange(R // 32), np.arange(C), indexing="ij")
+    assert np.array_equal(sc[_atom_byte(c, rb, (R + 127) // 128)], cs)
+
+
+def test_dual_rows_limit_leaves_the_rest():
+    bits = _draw(256, 128, 9)
+    qr, sr, qc, sc = _dual(bits, rows_limit=96)
+    x = bf16_bits_to_f32(bits[:96])
+    rq, _ = O.quantize_mxfp8(x, 1)
+    cq, _ = O.quantize_mxfp8(x, 0)
+    assert np.array_equal(qr[:96], rq) and np.array_equal(qc[:96], cq)
+    assert (qr[96:] == 0xAB).all() and (qc[96:] == 0xAB).all()
