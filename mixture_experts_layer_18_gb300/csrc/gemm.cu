@@ -570,6 +570,9 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
   const int cl = blockIdx.x / C::PAIR, ncl = gridDim.x / C::PAIR;
   uint8_t* sb0 = stg + ew * 4096;
   uint8_t* sb1 = sb0 + 2048;
+  // write-once results (h13, A, Z, dXp, weight gradients) leave L2 first;
+  // dh13, re-read by the dX / dW13 tiles of the same launch, does not
+  const uint64_t pol_ef = l2_evict_first_policy();
   // the accumulator is released on the MMA-issuing CTA's barrier
   const uint32_t tempty_cl0 = C::PAIR == 2 ? mapa_shared(smem_u32(&tempty[0]), 0) : 0;
   const uint32_t tempty_cl1 = C::PAIR == 2 ? mapa_shared(smem_u32(&tempty[1]), 0) : 0;
@@ -620,11 +623,11 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
         stage_end();
         if (lane == 0) {
           if (z >= 0) {
-            tma_store_3d(&g.tmO, sb0, xc, yc, z);
-            tma_store_3d(&g.tmO, sb1, xc + 32, yc, z);
+            tma_store_3d_ef(&g.tmO, sb0, xc, yc, z, pol_ef);
+            tma_store_3d_ef(&g.tmO, sb1, xc + 32, yc, z, pol_ef);
           } else {
-            tma_store_2d(&g.tmO, sb0, xc, yc);
-            tma_store_2d(&g.tmO, sb1, xc + 32, yc);
+            tma_store_2d_ef(&g.tmO, sb0, xc, yc, pol_ef);
+            tma_store_2d_ef(&g.tmO, sb1, xc + 32, yc, pol_ef);
           }
           bulk_commit();
         }
@@ -684,11 +687,11 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
             if (lane == 0) {
               const int xc = ti.n0 + cb + 64 * h2;
               if (ti.kind == GK_DW) {
-                tma_store_3d(&g.tmO, sb0, xc, ti.m0 + q * 32, ti.e);
-                tma_store_3d(&g.tmO, sb1, xc + 32, ti.m0 + q * 32, ti.e);
+                tma_store_3d_ef(&g.tmO, sb0, xc, ti.m0 + q * 32, ti.e, pol_ef);
+                tma_store_3d_ef(&g.tmO, sb1, xc + 32, ti.m0 + q * 32, ti.e, pol_ef);
               } else {
-                tma_store_2d(&g.tmO, sb0, xc, yrow);
-                tma_store_2d(&g.tmO, sb1, xc + 32, yrow);
+                tma_store_2d_ef(&g.tmO, sb0, xc, yrow, pol_ef);
+                tma_store_2d_ef(&g.tmO, sb1, xc + 32, yrow, pol_ef);
               }
               bulk_commit();
             }
@@ -714,8 +717,8 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
             stage_bf16_row(sb1, lane, w);
             stage_end();
             if (lane == 0) {
-              tma_store_2d(&g.tmO2, sb0, ti.n0 + c, yrow);
-              tma_store_2d(&g.tmO2, sb1, g.I + ti.n0 + c, yrow);
+              tma_store_2d_ef(&g.tmO2, sb0, ti.n0 + c, yrow, pol_ef);
+              tma_store_2d_ef(&g.tmO2, sb1, g.I + ti.n0 + c, yrow, pol_ef);
               bulk_commit();
             }
           } else {
@@ -730,7 +733,7 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
           stage_bf16_row(sb0, lane, v);
           stage_end();
           if (lane == 0) {
-            tma_store_2d(&g.tmO, sb0, ti.n0 + c, yrow);
+            tma_store_2d_ef(&g.tmO, sb0, ti.n0 + c, yrow, pol_ef);
             bulk_commit();
           }
         } else {

@@ -154,150 +154,162 @@ __global__ void __launch_bounds__(256) quant_colwise_kernel(const __nv_bfloat16*
 // scale layout: row-wise (blocks of 32 along each row; MN = rows, K = the
 // C columns) and column-wise (blocks of 32 rows down each column; MN =
 // columns, K = rows, kgroups = ceil(R / 128)).  A block of 256 threads
-// stages a 64-row x 128-column tile (two 32-row blocks) in shared memory,
-// finds its 256 column-block maxima (one per thread) and its row-block
-// maxima (pairs of threads, one shuffle), then every thread encodes 16
-// consecutive elements of a row twice and writes each set of 16 codes with
-// one 16-byte store (eight threads cover a row: coalesced); the next tile's
-// loads are issued before this one is encoded.  Codes and scale bytes are those of the
-// two kernels above.  Rows at or past `rows` (a device value, e.g. the
-// padded row total) are neither read nor written; they start on a 32-row
-// boundary.  qc == nullptr skips the column-wise output.
+// stages 128-row x 128-column tiles in shared memory with asynchronous
+// copies, double-buffered (the next tile's copies are in flight while this
+// one is encoded).  Threads 0-127 each take a column pair of a 32-row block
+// (its 32 words in registers: maxima, codes, 2-byte stores down the
+// column, 64 contiguous bytes per warp and row); threads 128-255 each take
+// (row, 32-column block) tasks (16 words: maximum, codes, two 16-byte
+// stores).  Codes and scale bytes are those of the two kernels above.
+// Rows at or past `rows` (a device value, e.g. the padded row total) are
+// neither read nor written; they start on a 32-row boundary.  qc == nullptr
+// skips the column-wise output.
 // SRC: 0 = row r of src; 1 = token row assign_of_row[r] / k of src (the
 // dispatch gather; pad rows read as 0); 2 = the same gather, with the
 // column-wise encoding taken of gate[a] * row rounded to bf16 (the
 // gate-scaled gradient rows of the weight-gradient GEMM).
+constexpr int kDualRows = 128;                     // tile rows (32-row blocks of K)
+constexpr int kDualPitch = 68;                     // words per tile row (272 B)
+constexpr int kDualTileWords = kDualRows * kDualPitch;
+
+// 16-byte asynchronous copy global -> shared; src_bytes 0 writes zeros.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_prev() {   // all but the newest group landed
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
+// Running max of |x| over bf16 pairs: for non-negative bf16 values the bit
+// patterns order like the numbers, so clearing the sign bits and taking a
+// per-halfword unsigned max gives both maxima at once (finite and infinite
+// inputs; the same result as fmaxf of the absolute values).
+__device__ __forceinline__ uint32_t absmax2(uint32_t acc, uint32_t w) {
+  return __vmaxu2(acc, w & 0x7FFF7FFFu);
+}
+__device__ __forceinline__ float absmax_lo(uint32_t acc) { return __uint_as_float(acc << 16); }
+__device__ __forceinline__ float absmax_hi(uint32_t acc) { return __uint_as_float(acc & 0xFFFF0000u); }
+
+template <int SRC>
+size_t dual_smem_bytes() {
+  return (size_t)2 * kDualTileWords * 4 + 2 * kDualRows * 4;
+}
+
 template <int SRC>
 __global__ void __launch_bounds__(256, 4) quant_dual_kernel(
     const __nv_bfloat16* __restrict__ src, int R, int C, int ld, const int32_t* __restrict__ rows_dev,
     const int32_t* __restrict__ assign_of_row, int k, int n_assign, const float* __restrict__ gate,
     int32_t* status, uint8_t* __restrict__ qr, uint8_t* __restrict__ sr, uint8_t* __restrict__ qc,
     uint8_t* __restrict__ sc) {
-  constexpr int TR = 64;                             // tile rows (two 32-row blocks)
-  constexpr int PITCH = 68;                          // words per tile row (272 B)
-  __shared__ __align__(16) uint32_t tile[TR][PITCH];                  // TR rows x 128 bf16
-  __shared__ __align__(16) uint32_t tileg[SRC == 2 ? TR : 1][PITCH];  // bf16(gate * row)
-  __shared__ float s_cinv[2][128];                   // column-wise 2^-s per (row block, column)
+  constexpr int TR = kDualRows, PITCH = kDualPitch;
+  extern __shared__ __align__(16) uint32_t dsm[];
+  uint32_t (*tbuf)[TR][PITCH] = reinterpret_cast<uint32_t (*)[TR][PITCH]>(dsm);   // [2]
+  float* s_g = reinterpret_cast<float*>(dsm + 2 * kDualTileWords);   // [2][TR] gates (SRC 2)
   const int rows = rows_dev ? min(*rows_dev, R) : R;
   const int nct = C / 128, nrt = (rows + TR - 1) / TR;
   const int64_t ntiles = (int64_t)nrt * nct;
   const int64_t kg_rows = (R + 127) / 128;
-  // this thread's four 16-byte chunks of a tile (and, gathered, their gate)
-  uint4 v[4];
-  float gv[4];
-  auto fetch = [&](int64_t t) {
+  // issue this thread's 16-byte copies of tile t into buffer b
+  auto issue = [&](int64_t t, int b) {
     const int rt = (int)(t / nct), ct = (int)(t - (int64_t)rt * nct);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < TR / 16; ++i) {
       const int ch = threadIdx.x + 256 * i;
-      const int r = rt * TR + (ch >> 4), c = ch & 15;
-      v[i] = make_uint4(0, 0, 0, 0);
-      gv[i] = 0.f;
+      const int rl = ch >> 4, c = ch & 15;
+      const int r = rt * TR + rl;
+      const __nv_bfloat16* p = src;
+      int bytes = 0;
       if (r < rows) {
         if constexpr (SRC == 0) {
-          v[i] = __ldg(reinterpret_cast<const uint4*>(src + (size_t)r * ld + ct * 128) + c);
+          p = src + (size_t)r * ld + ct * 128 + 8 * c;
+          bytes = 16;
         } else {
           const int a = assign_of_row[r];
           const bool ok = a >= 0 && a < n_assign;
           if (a >= n_assign && c == 0) report(status, MOE_ERR_BAD_INDEX);
           if (ok) {
-            v[i] = __ldg(reinterpret_cast<const uint4*>(src + (size_t)(a / k) * ld + ct * 128) + c);
-            if constexpr (SRC == 2) gv[i] = gate[a];
+            p = src + (size_t)(a / k) * ld + ct * 128 + 8 * c;
+            bytes = 16;
           }
+          if (SRC == 2 && c == 0) s_g[b * TR + rl] = ok ? gate[a] : 0.f;
         }
       }
+      cp_async16(&tbuf[b][rl][4 * c], p, bytes);
     }
   };
   int64_t t = blockIdx.x;
-  if (t < ntiles) fetch(t);
-  for (; t < ntiles; t += gridDim.x) {
+  if (t < ntiles) issue(t, 0);
+  cp_async_commit();
+  for (int b = 0; t < ntiles; t += gridDim.x, b ^= 1) {
     const int rt = (int)(t / nct), ct = (int)(t - (int64_t)rt * nct);
     const int r0 = rt * TR, c0 = ct * 128;
-    const int nrb = min(TR, rows - r0) / 32;        // 32-row blocks of this tile (1 or 2)
-    __syncthreads();   // previous tile fully consumed
+    const int nrb = min(TR, rows - r0) / 32;        // 32-row blocks of this tile
+    if (t + gridDim.x < ntiles) issue(t + gridDim.x, b ^ 1);   // next tile in flight
+    cp_async_commit();
+    cp_async_wait_prev();
+    __syncthreads();   // tile t in buffer b, from every thread's copies
+    const uint32_t (*tile)[PITCH] = tbuf[b];
+    if (threadIdx.x < 128) {
+      // column-wise: thread = (32-row block, column pair); the 32 words of
+      // its two columns in registers, maxima and codes from them
+      for (int rb = threadIdx.x >> 6; rb < nrb; rb += 2) {
+        if (!qc) break;
+        const int j = threadIdx.x & 63;
+        uint32_t w[32];
+        uint32_t acc = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int ch = threadIdx.x + 256 * i;
-      const int r = ch >> 4, c = ch & 15;
-      *reinterpret_cast<uint4*>(&tile[r][4 * c]) = v[i];
-      if constexpr (SRC == 2) {
-        const float g = gv[i];
-        *reinterpret_cast<uint4*>(&tileg[r][4 * c]) =
-            make_uint4(pack_bf16(g * bf16_lo(v[i].x), g * bf16_hi(v[i].x)),
-                       pack_bf16(g * bf16_lo(v[i].y), g * bf16_hi(v[i].y)),
-                       pack_bf16(g * bf16_lo(v[i].z), g * bf16_hi(v[i].z)),
-                       pack_bf16(g * bf16_lo(v[i].w), g * bf16_hi(v[i].w)));
-      }
-    }
-    __syncthreads();
-    if (t + gridDim.x < ntiles) fetch(t + gridDim.x);   // next tile's loads overlap this one
-    const uint32_t (*ctile)[PITCH] = SRC == 2 ? tileg : tile;   // column-wise source
-    // column maxima: thread = (row block, column)
-    if (qc) {
-      const int rb = threadIdx.x >> 7, c = threadIdx.x & 127;
-      if (rb < nrb) {
-        float am = 0.f;
-#pragma unroll 8
         for (int r = 0; r < 32; ++r) {
-          const uint32_t w = ctile[32 * rb + r][c >> 1];
-          am = fmaxf(am, fabsf((c & 1) ? bf16_hi(w) : bf16_lo(w)));
+          w[r] = tile[32 * rb + r][j];
+          if constexpr (SRC == 2) {   // gate-scaled rows, rounded to bf16 once
+            const float g = s_g[b * TR + 32 * rb + r];
+            w[r] = pack_bf16(g * bf16_lo(w[r]), g * bf16_hi(w[r]));
+          }
+          acc = absmax2(acc, w[r]);
         }
-        const int sb = mx_scale_byte(am);
-        s_cinv[rb][c] = mx_inv_scale(sb);
-        sc[mma_scale_index(c0 + c, (r0 >> 5) + rb, kg_rows)] = (uint8_t)sb;
+        const int sb0 = mx_scale_byte(absmax_lo(acc)), sb1 = mx_scale_byte(absmax_hi(acc));
+        const float inv0 = mx_inv_scale(sb0), inv1 = mx_inv_scale(sb1);
+        uint16_t* d = reinterpret_cast<uint16_t*>(qc + (size_t)(r0 + 32 * rb) * C + c0 + 2 * j);
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+          d[(size_t)r * (C / 2)] = e4m3x2(bf16_lo(w[r]) * inv0, bf16_hi(w[r]) * inv1);
+        sc[mma_scale_index(c0 + 2 * j, (r0 >> 5) + rb, kg_rows)] = (uint8_t)sb0;
+        sc[mma_scale_index(c0 + 2 * j + 1, (r0 >> 5) + rb, kg_rows)] = (uint8_t)sb1;
       }
-    }
-    // row-wise: thread = (row, 16-column group); it and its neighbour
-    // (group ^ 1) form one 32-column block
-#pragma unroll
-    for (int p = 0; p < 2; ++p) {
-      const int er = (threadIdx.x >> 3) + 32 * p, eg = threadIdx.x & 7;
-      if (er >= 32 * nrb) break;
-      uint32_t w[8];
-      const uint4 v0 = *reinterpret_cast<const uint4*>(&tile[er][8 * eg]);
-      const uint4 v1 = *reinterpret_cast<const uint4*>(&tile[er][8 * eg + 4]);
-      w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
-      w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
-      float am = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) am = fmaxf(am, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
-      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-      const int sb = mx_scale_byte(am);
-      const float inv = mx_inv_scale(sb);
-      uint32_t o[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t p0 = e4m3x2(bf16_lo(w[2 * i]) * inv, bf16_hi(w[2 * i]) * inv);
-        const uint32_t p1 = e4m3x2(bf16_lo(w[2 * i + 1]) * inv, bf16_hi(w[2 * i + 1]) * inv);
-        o[i] = p0 | (p1 << 16);
-      }
-      *reinterpret_cast<uint4*>(qr + (size_t)(r0 + er) * C + c0 + 16 * eg) =
-          make_uint4(o[0], o[1], o[2], o[3]);
-      if ((eg & 1) == 0) sr[mma_scale_index(r0 + er, (c0 >> 5) + (eg >> 1), nct)] = (uint8_t)sb;
-    }
-    if (qc) {
-      __syncthreads();   // column scales ready
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        const int er = (threadIdx.x >> 3) + 32 * p, eg = threadIdx.x & 7;
-        if (er >= 32 * nrb) break;
-        uint32_t w[8];
-        const uint4 v0 = *reinterpret_cast<const uint4*>(&ctile[er][8 * eg]);
-        const uint4 v1 = *reinterpret_cast<const uint4*>(&ctile[er][8 * eg + 4]);
-        w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
-        w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
-        uint32_t o[4];
+    } else {
+      // row-wise: thread = (row, 32-column block), tile rows x 4 tasks over
+      // threads 128-255
+      for (int task = threadIdx.x - 128; task < 32 * nrb * 4; task += 128) {
+        const int er = task >> 2, bb = task & 3;
+        uint32_t w[16];
+        uint32_t acc = 0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float* ci = &s_cinv[p][16 * eg + 4 * i];
-          o[i] = (uint32_t)e4m3x2(bf16_lo(w[2 * i]) * ci[0], bf16_hi(w[2 * i]) * ci[1]) |
-                 ((uint32_t)e4m3x2(bf16_lo(w[2 * i + 1]) * ci[2], bf16_hi(w[2 * i + 1]) * ci[3]) << 16);
+          const uint4 v = *reinterpret_cast<const uint4*>(&tile[er][16 * bb + 4 * i]);
+          w[4 * i + 0] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
         }
-        *reinterpret_cast<uint4*>(qc + (size_t)(r0 + er) * C + c0 + 16 * eg) =
-            make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc = absmax2(acc, w[i]);
+        const int sbv = mx_scale_byte(fmaxf(absmax_lo(acc), absmax_hi(acc)));
+        const float inv = mx_inv_scale(sbv);
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t p0 = e4m3x2(bf16_lo(w[2 * i]) * inv, bf16_hi(w[2 * i]) * inv);
+          const uint32_t p1 = e4m3x2(bf16_lo(w[2 * i + 1]) * inv, bf16_hi(w[2 * i + 1]) * inv);
+          o[i] = p0 | (p1 << 16);
+        }
+        uint4* d = reinterpret_cast<uint4*>(qr + (size_t)(r0 + er) * C + c0 + 32 * bb);
+        d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        sr[mma_scale_index(r0 + er, (c0 >> 5) + bb, nct)] = (uint8_t)sbv;
       }
     }
+    __syncthreads();   // buffer b and its gates are free for the next tiles
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 int grid_cap() {
@@ -336,22 +348,54 @@ cudaError_t launch_quantize(const void* src, int R, int C, int ld, int axis,
 cudaError_t launch_quantize_dual(const void* src, int R, int C, int ld, const int32_t* rows_dev,
                                  uint8_t* qr, uint8_t* sr, uint8_t* qc, uint8_t* sc,
                                  cudaStream_t s, const DualGather* gather) {
-  const int64_t tiles = (int64_t)((R + 63) / 64) * (C / 128);
+  const int64_t tiles = (int64_t)((R + kDualRows - 1) / kDualRows) * (C / 128);
   if (tiles == 0) return cudaSuccess;
-  const int cap = grid_cap();
-  const int blocks = (int)(tiles < cap ? tiles : cap);
   const __nv_bfloat16* x = (const __nv_bfloat16*)src;
-  if (!gather)
-    quant_dual_kernel<0><<<blocks, 256, 0, s>>>(x, R, C, ld, rows_dev, nullptr, 1, 0, nullptr,
-                                                nullptr, qr, sr, qc, sc);
-  else if (!gather->gate)
-    quant_dual_kernel<1><<<blocks, 256, 0, s>>>(x, R, C, ld, rows_dev, gather->assign_of_row,
-                                                gather->k, gather->n_assign, nullptr,
-                                                gather->status, qr, sr, qc, sc);
-  else
-    quant_dual_kernel<2><<<blocks, 256, 0, s>>>(x, R, C, ld, rows_dev, gather->assign_of_row,
-                                                gather->k, gather->n_assign, gather->gate,
-                                                gather->status, qr, sr, qc, sc);
+  // per device (the attribute belongs to a context): shared-memory opt-in
+  // and the resident block count, so the grid is exactly one wave and every
+  // block strides over the same number of tiles
+  static bool attr_set[64][3] = {};
+  static int resident[64][3] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  bool* attr_done = attr_set[dev];
+  int blocks = 0;
+  auto setup = [&](auto kern, size_t bytes, int which) {
+    if (!attr_done[which]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+          cudaSuccess)
+        return false;
+      int per_sm = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, bytes) != cudaSuccess ||
+          per_sm < 1)
+        return false;
+      int sms = 0;
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      resident[dev][which] = per_sm * (sms > 0 ? sms : 1);
+      attr_done[which] = true;
+    }
+    blocks = (int)(tiles < resident[dev][which] ? tiles : resident[dev][which]);
+    return true;
+  };
+  if (!gather) {
+    const size_t sm = dual_smem_bytes<0>();
+    if (!setup(quant_dual_kernel<0>, sm, 0)) return cudaErrorInvalidValue;
+    quant_dual_kernel<0><<<blocks, 256, sm, s>>>(x, R, C, ld, rows_dev, nullptr, 1, 0, nullptr,
+                                                 nullptr, qr, sr, qc, sc);
+  } else if (!gather->gate) {
+    const size_t sm = dual_smem_bytes<1>();
+    if (!setup(quant_dual_kernel<1>, sm, 1)) return cudaErrorInvalidValue;
+    quant_dual_kernel<1><<<blocks, 256, sm, s>>>(x, R, C, ld, rows_dev, gather->assign_of_row,
+                                                 gather->k, gather->n_assign, nullptr,
+                                                 gather->status, qr, sr, qc, sc);
+  } else {
+    const size_t sm = dual_smem_bytes<2>();
+    if (!setup(quant_dual_kernel<2>, sm, 2)) return cudaErrorInvalidValue;
+    quant_dual_kernel<2><<<blocks, 256, sm, s>>>(x, R, C, ld, rows_dev, gather->assign_of_row,
+                                                 gather->k, gather->n_assign, gather->gate,
+                                                 gather->status, qr, sr, qc, sc);
+  }
   return cudaGetLastError();
 }
 
