@@ -199,7 +199,7 @@ size_t dual_smem_bytes() {
 }
 
 template <int SRC>
-__global__ void __launch_bounds__(256, 4) quant_dual_kernel(
+__global__ void __launch_bounds__(256, 3) quant_dual_kernel(
     const __nv_bfloat16* __restrict__ src, int R, int C, int ld, const int32_t* __restrict__ rows_dev,
     const int32_t* __restrict__ assign_of_row, int k, int n_assign, const float* __restrict__ gate,
     int32_t* status, uint8_t* __restrict__ qr, uint8_t* __restrict__ sr, uint8_t* __restrict__ qc,
@@ -212,42 +212,73 @@ __global__ void __launch_bounds__(256, 4) quant_dual_kernel(
   const int nct = C / 128, nrt = (rows + TR - 1) / TR;
   const int64_t ntiles = (int64_t)nrt * nct;
   const int64_t kg_rows = (R + 127) / 128;
-  // issue this thread's 16-byte copies of tile t into buffer b
+  // Gathered tiles: the assignment (and gate) of each of this thread's rows
+  // is loaded one tile ahead of its copies, so issuing a tile's copies never
+  // waits on the index load.
+  constexpr int NCH = TR / 16;                     // 16-byte chunks per thread per tile
+  int ai[NCH];
+  float gi[NCH];
+  auto load_rows = [&](int64_t t) {
+    const int rt = (int)(t / nct);
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      const int r = rt * TR + ((threadIdx.x + 256 * i) >> 4);
+      ai[i] = -1;
+      gi[i] = 0.f;
+      if constexpr (SRC != 0) {
+        if (r < rows) {
+          const int a = assign_of_row[r];
+          const int c = (threadIdx.x + 256 * i) & 15;
+          if (a >= n_assign && c == 0) report(status, MOE_ERR_BAD_INDEX);
+          if (a >= 0 && a < n_assign) {
+            ai[i] = a;
+            if constexpr (SRC == 2) gi[i] = gate[a];
+          }
+        }
+      }
+    }
+  };
+  // issue this thread's 16-byte copies of tile t into buffer b (gathered:
+  // rows from ai / gi, loaded by load_rows(t))
   auto issue = [&](int64_t t, int b) {
     const int rt = (int)(t / nct), ct = (int)(t - (int64_t)rt * nct);
 #pragma unroll
-    for (int i = 0; i < TR / 16; ++i) {
+    for (int i = 0; i < NCH; ++i) {
       const int ch = threadIdx.x + 256 * i;
       const int rl = ch >> 4, c = ch & 15;
       const int r = rt * TR + rl;
       const __nv_bfloat16* p = src;
       int bytes = 0;
-      if (r < rows) {
-        if constexpr (SRC == 0) {
+      if constexpr (SRC == 0) {
+        if (r < rows) {
           p = src + (size_t)r * ld + ct * 128 + 8 * c;
           bytes = 16;
-        } else {
-          const int a = assign_of_row[r];
-          const bool ok = a >= 0 && a < n_assign;
-          if (a >= n_assign && c == 0) report(status, MOE_ERR_BAD_INDEX);
-          if (ok) {
-            p = src + (size_t)(a / k) * ld + ct * 128 + 8 * c;
-            bytes = 16;
-          }
-          if (SRC == 2 && c == 0) s_g[b * TR + rl] = ok ? gate[a] : 0.f;
         }
+      } else {
+        if (ai[i] >= 0) {
+          p = src + (size_t)(ai[i] / k) * ld + ct * 128 + 8 * c;
+          bytes = 16;
+        }
+        if (SRC == 2 && c == 0) s_g[b * TR + rl] = gi[i];
       }
       cp_async16(&tbuf[b][rl][4 * c], p, bytes);
     }
   };
   int64_t t = blockIdx.x;
-  if (t < ntiles) issue(t, 0);
+  if (t < ntiles) {
+    load_rows(t);
+    issue(t, 0);
+    if (t + gridDim.x < ntiles) load_rows(t + gridDim.x);
+  }
   cp_async_commit();
   for (int b = 0; t < ntiles; t += gridDim.x, b ^= 1) {
     const int rt = (int)(t / nct), ct = (int)(t - (int64_t)rt * nct);
     const int r0 = rt * TR, c0 = ct * 128;
     const int nrb = min(TR, rows - r0) / 32;        // 32-row blocks of this tile
-    if (t + gridDim.x < ntiles) issue(t + gridDim.x, b ^ 1);   // next tile in flight
+    if (t + gridDim.x < ntiles) {
+      issue(t + gridDim.x, b ^ 1);                 // next tile's copies in flight
+      if (t + 2 * (int64_t)gridDim.x < ntiles) load_rows(t + 2 * (int64_t)gridDim.x);
+    }
     cp_async_commit();
     cp_async_wait_prev();
     __syncthreads();   // tile t in buffer b, from every thread's copies

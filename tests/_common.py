@@ -50,3 +50,11 @@ def rel_err(got, ref):
     if den == 0:
         return float(np.abs(got).max())
     return float(np.abs(got - ref).max() / den)
+
+
+def atom_byte(mn, kb, kgroups):
+    """Byte of (MN index, 32-element K block) in the tensor-core scale atoms
+    (512-byte atoms of 128 MN indices x 4 K blocks), as declared in moe.h."""
+    mn = np.asarray(mn)
+    kb = np.asarray(kb)
+    return ((mn // 128) * kgroups + kb // 4) * 512 + (mn % 32) * 16 + ((mn // 32) % 4) * 4 + kb % 4

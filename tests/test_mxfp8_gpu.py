@@ -8,7 +8,7 @@ import pytest
 from oracle import moe_oracle as O
 from workloads import CONFIGS, MoEConfig, make_inputs
 
-from _common import TOL_BF16, TOL_MXFP8, F32View, rel_err, to_device, to_f64
+from _common import TOL_BF16, TOL_MXFP8, F32View, atom_byte, rel_err, to_device, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -94,6 +94,40 @@ def test_pair_and_single_cta_agree_bitwise():
             assert rel_err(to_f64(a[k]), to_f64(b[k])) <= 1e-6, k
         else:
             assert torch.equal(a[k], b[k]), k
+
+
+def test_saved_encodings_bit_exact():
+    """The mxfp8 forward leaves in `saved` the backward's encodings of
+    X_perm (gathered and quantised in one pass, 32-row blocks per expert
+    group) and of W13 / W2 (row-wise, from the same passes as the forward's
+    column-wise ones).  Codes and scale bytes equal the oracle's quantiser
+    applied to the oracle's own permutation of X and to the weights."""
+    from workloads import bf16_bits_to_f32
+    cfg = SMALL[2]
+    inp = make_inputs(cfg, 6)
+    L, _ = _run(cfg, inp, "mxfp8")
+    lay, sv = L.layout, L.saved.cpu().numpy()
+    rows = L.max_rows
+    rp = (rows + 127) // 128 * 128
+    H, I, E, k = cfg.H, cfg.I, cfg.E, cfg.k
+    idx, _ = O.route(inp["logits"], k)
+    pm = O.permute(idx, E)
+    tpad = int(pm["padded_offsets"][-1])
+    X = bf16_bits_to_f32(inp["X"]).astype(np.float64)
+    aor = pm["assign_of_row"]
+    xperm = np.zeros((tpad, H))
+    xperm[aor >= 0] = X[aor[aor >= 0] // k]
+    cq, cs = O.quantize_mxfp8(xperm, 0, pm["padded_offsets"])
+    q = sv[lay.x_col_q: lay.x_col_q + rows * H].reshape(rows, H)[:tpad]
+    assert np.array_equal(q, cq)
+    rb, c = np.meshgrid(np.arange(tpad // 32), np.arange(H), indexing="ij")
+    assert np.array_equal(sv[lay.x_col_sf + atom_byte(c, rb, rp // 128)], cs)
+    for name, W, R, C in (("w13_row", inp["W13"], E * H, 2 * I), ("w2_row", inp["W2"], E * I, H)):
+        rq, rs = O.quantize_mxfp8(bf16_bits_to_f32(W).reshape(R, C).astype(np.float64), 1)
+        off_q, off_s = getattr(lay, name + "_q"), getattr(lay, name + "_sf")
+        assert np.array_equal(sv[off_q: off_q + R * C].reshape(R, C), rq), name
+        r, kb = np.meshgrid(np.arange(R), np.arange(C // 32), indexing="ij")
+        assert np.array_equal(sv[off_s + atom_byte(r, kb, C // 128)], rs), name
 
 
 @pytest.mark.parametrize("mode", ["mxfp8", "fp8_bwd"])

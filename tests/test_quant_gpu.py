@@ -10,6 +10,8 @@ import mixture_experts_layer_18_gb300 as M
 from oracle import moe_oracle as O
 from workloads import bf16_bits_to_f32, f32_to_bf16_bits
 
+from _common import atom_byte
+
 pytestmark = pytest.mark.gpu
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -108,14 +110,6 @@ def test_golden_blocks_on_gpu():
         assert list(q[i, : len(want)]) == want, case["name"]
 
 
-def _atom_byte(mn, kb, kgroups):
-    """Byte of (MN index, 32-element K block) in the tensor-core scale atoms
-    (512-byte atoms of 128 MN indices x 4 K blocks), as declared in moe.h."""
-    mn = np.asarray(mn)
-    kb = np.asarray(kb)
-    return ((mn // 128) * kgroups + kb // 4) * 512 + (mn % 32) * 16 + ((mn // 32) % 4) * 4 + kb % 4
-
-
 def _dual(bits, rows_limit=None):
     import torch
     R, C = bits.shape
@@ -148,9 +142,9 @@ def test_dual_bit_exact(R, C):
     assert np.array_equal(qr, rq)
     assert np.array_equal(qc, cq)
     r, kb = np.meshgrid(np.arange(R), np.arange(C // 32), indexing="ij")
-    assert np.array_equal(sr[_atom_byte(r, kb, C // 128)], rs)
+    assert np.array_equal(sr[atom_byte(r, kb, C // 128)], rs)
     rb, c = np.meshgrid(np.arange(R // 32), np.arange(C), indexing="ij")
-    assert np.array_equal(sc[_atom_byte(c, rb, (R + 127) // 128)], cs)
+    assert np.array_equal(sc[atom_byte(c, rb, (R + 127) // 128)], cs)
 
 
 def test_dual_rows_limit_leaves_the_rest():
