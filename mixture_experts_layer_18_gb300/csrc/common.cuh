@@ -160,6 +160,13 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
       : "memory");
 }
 
+// Hint: bring `bytes` bytes at p (16-byte aligned, a multiple of 16) into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(bytes)
+               : "memory");
+}
+
 // Bulk tensor stores shared -> global (bulk-group completion).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* smem_src, int x,
                                              int y) {
@@ -438,6 +445,23 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   d |= (uint64_t)1 << 46;   // descriptor version for tcgen05
   d |= (uint64_t)2 << 61;   // SWIZZLE_128B
   return d;
+}
+
+// Copy two runs of 32 fp32 columns (at src0 and src1) of the warp's 32 TMEM
+// lanes to 64 consecutive columns at dst (src0's run first).  The values
+// pass through registers that live only inside this statement; both waits
+// are included, so the sources may be overwritten and dst read afterwards.
+__device__ __forceinline__ void tmem_move32x2(uint32_t src0, uint32_t src1, uint32_t dst) {
+  asm volatile(
+      "{\n .reg .b32 r<64>;\n"
+      " tcgen05.ld.sync.aligned.32x32b.x32.b32 {r0,r1,r2,r3,r4,r5,r6,r7,r8,r9,r10,r11,r12,r13,r14,r15,r16,r17,r18,r19,r20,r21,r22,r23,r24,r25,r26,r27,r28,r29,r30,r31}, [%0];\n"
+      " tcgen05.ld.sync.aligned.32x32b.x32.b32 {r32,r33,r34,r35,r36,r37,r38,r39,r40,r41,r42,r43,r44,r45,r46,r47,r48,r49,r50,r51,r52,r53,r54,r55,r56,r57,r58,r59,r60,r61,r62,r63}, [%1];\n"
+      " tcgen05.wait::ld.sync.aligned;\n"
+      " tcgen05.st.sync.aligned.32x32b.x32.b32 [%2], {r0,r1,r2,r3,r4,r5,r6,r7,r8,r9,r10,r11,r12,r13,r14,r15,r16,r17,r18,r19,r20,r21,r22,r23,r24,r25,r26,r27,r28,r29,r30,r31};\n"
+      " tcgen05.st.sync.aligned.32x32b.x32.b32 [%3], {r32,r33,r34,r35,r36,r37,r38,r39,r40,r41,r42,r43,r44,r45,r46,r47,r48,r49,r50,r51,r52,r53,r54,r55,r56,r57,r58,r59,r60,r61,r62,r63};\n"
+      " tcgen05.wait::st.sync.aligned;\n}"
+      ::"r"(src0), "r"(src1), "r"(dst), "r"(dst + 32)
+      : "memory");
 }
 
 // ------------------------------------------------------------- bf16 utils

@@ -136,6 +136,13 @@ struct Cfg {
                                     1024 /*align*/ + 256 /*bars*/ + 2 * (kMaxE + 1) * 4 + 512 + 64;
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
   static_assert(!MX || SF_COL0 + STAGES * 16 <= 512, "TMEM scale slots");
+  // Block-scaled pairs: the last 128 columns hold, per lane quarter, the
+  // second half of both epilogue warps' columns (64 each), moved out of the
+  // accumulator so it can be released half-way through the gate/up and D
+  // epilogues.
+  static constexpr bool SPLIT = MX && PAIR == 2;
+  static constexpr int SPARE_COL = 384;
+  static_assert(!SPLIT || SF_COL0 + STAGES * 16 <= SPARE_COL, "TMEM spare columns");
 };
 
 // ------------------------------------------------------------ tile decode
@@ -600,6 +607,14 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
     const Elt* h13a = nullptr;
     if (ti.kind == GK_BWD_D && ti.valid) {
       h13a = static_cast<const Elt*>(g.aux) + (size_t)(ti.m0 + r) * g.ld_aux + ti.n0;
+      // the row's u and v columns of this tile reach L2 while its MMAs run
+      const int ncol = min(cw, g.I - (ti.n0 + cb));
+      const uint32_t pbytes = ncol > 0 ? ((uint32_t)ncol * (uint32_t)sizeof(Elt)) & ~15u : 0u;
+      if (pbytes) {
+        if ((reinterpret_cast<uintptr_t>(h13a + cb) & 15) == 0) prefetch_l2_bulk(h13a + cb, pbytes);
+        if ((reinterpret_cast<uintptr_t>(h13a + g.I + cb) & 15) == 0)
+          prefetch_l2_bulk(h13a + g.I + cb, pbytes);
+      }
       load_raw<Elt, NV>(h13a + cb, pu);
       load_raw<Elt, NV>(h13a + g.I + cb, pv);
     }
@@ -637,6 +652,18 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       }
     };
     bool released = false;
+    // gate/up and D on block-scaled pairs: the second half of this warp's
+    // columns is moved to the spare TMEM columns, and the accumulator is
+    // released once the first half has been read
+    auto spare_col = [&](int c) {
+      return tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(C::SPARE_COL + h * 64 + c);
+    };
+    auto release_now = [&]() {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(buf ? tempty_cl1 : tempty_cl0);
+      released = true;
+    };
     if constexpr (C::EPI_WARPS == 8) {
       // Block-scaled pairs hold their only accumulator until it is
       // released: for the plain kinds the warp's 128 columns are read and
@@ -707,9 +734,15 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       const int row = ti.m0 + r;
       Elt* outA = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
       Elt* h13 = g.out2 ? static_cast<Elt*>(g.out2) + (size_t)row * g.ld_out2 + ti.n0 : nullptr;
+      const int half = cb + cw / 2;
+      if constexpr (C::SPLIT) tmem_move32x2(taddr + half, taddr + C::BN / 2 + half, spare_col(0));
 #pragma unroll 1
       for (int c = cb; c < cb + cw; c += 32) {
-        tmem_ld32x2(taddr + c, taddr + C::BN / 2 + c, v, w);   // u: gate half, v: up half
+        if (C::SPLIT && c == half) release_now();
+        if (C::SPLIT && c >= half)
+          tmem_ld32x2(spare_col(c - half), spare_col(c - half + 32), v, w);
+        else
+          tmem_ld32x2(taddr + c, taddr + C::BN / 2 + c, v, w);   // u: gate half, v: up half
         if (h13) {
           if constexpr (TS) {
             stage_begin();
@@ -766,16 +799,23 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       const float gt = a >= 0 ? g.gate[a] : 0.f;
       Elt* dh = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
       float part = 0.f;
+      const int half = cb + cw / 2;
+      if constexpr (C::SPLIT) tmem_move32x2(taddr + half, taddr + half + 32, spare_col(0));
+      uint32_t src = taddr + cb;               // TMEM columns of the next chunk
 #pragma unroll 1
-      for (int c = cb; c < cb + cw; c += 32) {
+      for (int c = cb; c < cb + cw; c += 32, src += 32) {
         float D[32];
+        if (C::SPLIT && c == half) {
+          release_now();
+          src = spare_col(0);
+        }
         unpack_raw<Elt, NV>(pu, v);            // u of this chunk
         unpack_raw<Elt, NV>(pv, w);            // v of this chunk
         if (c + 32 < cb + cw) {                // fetch the next chunk while this one runs
           load_raw<Elt, NV>(h13a + c + 32, pu);
           load_raw<Elt, NV>(h13a + g.I + c + 32, pv);
         }
-        tmem_ld32(taddr + c, D);
+        tmem_ld32(src, D);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float u = v[i], vv = w[i];
