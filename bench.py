@@ -36,16 +36,14 @@ import numpy as np  # noqa: E402
 
 from workloads import CONFIGS, make_inputs  # noqa: E402
 
-# kernels launched per step: route 3; forward 4 (+4 quantise passes in
-# mxfp8); backward 4 (+8 quantise passes and a second GEMM launch with MXFP8
-# gradients); router backward 1
 # Kernels of this library per timed step (route 3: router, scan, scatter;
 # router backward 1).  bf16: forward gather, 2 GEMMs, combine; backward
-# gather, 1 co-scheduled GEMM launch, combine, d(gate) reduction.  mxfp8:
-# forward gather+quantise, W13 / A / W2 dual quantise, 2 GEMMs, combine;
-# backward dY gather+quantise, 2 GEMM launches, dh13 dual quantise,
-# combine, d(gate) reduction.  fp8_bwd: the bf16 forward, and the mxfp8
-# backward plus 4 quantise passes of W2, A, W13, X_perm.
+# gather of dY, 1 co-scheduled GEMM launch, combine, d(gate) reduction.
+# mxfp8: forward gather+quantise, W13 / A / W2 dual quantise, 2 GEMMs,
+# combine; backward dY gather+quantise, 2 GEMM launches, dh13 dual
+# quantise, combine, d(gate) reduction.  fp8_bwd: the bf16-precision
+# forward (gate after W2), and the mxfp8 backward plus 4 quantise passes of
+# W2, A, W13, X_perm.
 LAUNCHES_PER_STEP = {"bf16": 12, "mxfp8": 17, "fp8_bwd": 18}
 CPU_SAMPLE_EXPERTS = 16   # cpu_baseline: all assignments of 16 experts
 REF_SAMPLE_EXPERTS = 1    # reference arm: one expert per step (rotating)

@@ -103,11 +103,13 @@ typedef struct {
 /* Byte offsets of the tensors inside the `saved` buffer written by
  * moe_forward and read by moe_backward (rows = moe_max_rows(dims), elem =
  * 4 bytes for MOE_F32, else 2):
- *   x_perm [rows, H]   gathered tokens, expert-major, zero pad rows (not
- *                      written in MOE_MXFP8 mode: the dispatch gather goes
- *                      straight into its MXFP8 encodings, x_col below)
+ *   x_perm [rows, H]   gathered tokens, expert-major, zero pad rows
+ *                      (zero-sized in MOE_MXFP8 mode: the dispatch gather
+ *                      goes straight into its MXFP8 encodings, x_col below)
  *   h13    [rows, 2I]  X_perm_e W13_e before the activation (if save_for_backward)
- *   act    [rows, I]   A = silu(h13[:, :I]) * h13[:, I:]
+ *   act    [rows, I]   A = silu(h13[:, :I]) * h13[:, I:]; in MOE_BF16 mode
+ *                      gate * A (the gate of the row's assignment, 0 on pad
+ *                      rows), the form both the down GEMM and dW2 consume
  * MOE_MXFP8 only (zero-sized in the other modes): the backward's MXFP8
  * operands, which the forward quantises in the same passes as its own
  * (E4M3 codes *_q, tensor-core scale atoms *_sf; written only with
@@ -186,6 +188,8 @@ moe_status moe_route_backward(const moe_dims* dims, const moe_route_out* route,
  *   A      = silu(h13[:, :I]) * h13[:, I:]           (fused epilogue)
  *   Z      = gate * (A_e W2_e)                        (grouped GEMM + gate)
  *   Y[t]   = sum_j Z[row_of_assign[t*k + j]]          (deterministic combine)
+ * In MOE_BF16 mode the gate is applied to A in the gate/up epilogue instead
+ * (Z = (gate * A_e) W2_e, the same product).
  *   X    [T, H]; W13 [E, H, 2I]; W2 [E, I, H]; Y [T, H]  (device)
  *   route  moe_route output for the same dims.
  *   saved  moe_saved_layout_of(dims).total bytes (device).
@@ -204,7 +208,9 @@ moe_status moe_forward(const moe_dims* dims, const void* X, const void* W13,
  *   dW13_e = X_perm_e^T dh13_e,  dW2_e = A_e^T (gate * dY)_perm_e,
  * experts with no token get zero weight gradients.  The activation-gradient
  * GEMMs and the weight-gradient GEMMs run as co-scheduled tiles of one
- * persistent launch.
+ * persistent launch.  In MOE_BF16 mode dW2_e = (gate * A)_e^T dY_perm_e (the
+ * same product, from the gated `act` the forward saved: no gated copy of dY
+ * is made).
  *   dY [T, H]; dX [T, H]; dW13 [E, H, 2I]; dW2 [E, I, H]; dgate float [T, k]
  *   saved  the buffer written by moe_forward with save_for_backward = 1.
  *   ws     MOE_WS_BACKWARD workspace. */

@@ -19,24 +19,64 @@ constexpr int kThreads = 256;
 __device__ __forceinline__ int grid_warps() { return (gridDim.x * blockDim.x) >> 5; }
 __device__ __forceinline__ int global_warp() { return (blockIdx.x * blockDim.x + threadIdx.x) >> 5; }
 
-// dst[r] = src[assign_of_row[r] / k] for r < padded_offsets[E]; pad rows 0.
-// One warp per row, 16-byte vectors.
-__global__ void __launch_bounds__(kThreads) gather_rows_kernel(
-    const uint4* __restrict__ src, uint4* __restrict__ dst, int vec_per_row, int k,
-    int n_assign, const int32_t* __restrict__ assign_of_row,
-    const int32_t* __restrict__ padded_offsets, int E, int32_t* status) {
+// Dispatch in token order: dst[row_of_assign[t*k + j]] = src[t] for every
+// slot j, then pad rows (assign_of_row < 0) = 0.  A warp takes one
+// (token, 4 KB column chunk) unit: it reads the chunk once and writes it to
+// the token's k rows, so each source row crosses HBM once however far apart
+// the expert order puts its copies.
+constexpr int kDispatchNV = 8;   // 16-byte vectors per lane per unit
+__global__ void __launch_bounds__(kThreads) dispatch_rows_kernel(
+    const uint4* __restrict__ src, uint4* __restrict__ dst, int vec_per_row, int T, int k,
+    int n_assign, const int32_t* __restrict__ row_of_assign,
+    const int32_t* __restrict__ assign_of_row, const int32_t* __restrict__ padded_offsets, int E,
+    int32_t* status) {
   const int rows = padded_offsets[E];
   const int lane = threadIdx.x & 31;
-  for (int r = global_warp(); r < rows; r += grid_warps()) {
-    const int a = assign_of_row[r];
-    uint4* d = dst + (size_t)r * vec_per_row;
-    if (a < 0 || a >= n_assign) {
-      if (a >= n_assign && lane == 0) report(status, MOE_ERR_BAD_INDEX);
-      for (int c = lane; c < vec_per_row; c += 32) d[c] = make_uint4(0, 0, 0, 0);
-      continue;
+  const int chunk = 32 * kDispatchNV;
+  const int nch = (vec_per_row + chunk - 1) / chunk;
+  const int64_t units = (int64_t)T * nch;
+  for (int64_t u = global_warp(); u < units; u += grid_warps()) {
+    const int t = (int)(u / nch);
+    const int c0 = (int)(u - (int64_t)t * nch) * chunk;
+    int my = -1;                       // lane j < k: destination row of slot j
+    if (lane < k) {
+      my = row_of_assign[(size_t)t * k + lane];
+      if (my < 0 || my >= rows) {
+        report(status, MOE_ERR_BAD_INDEX);
+        my = -1;
+      }
     }
-    const uint4* s = src + (size_t)(a / k) * vec_per_row;
-    for (int c = lane; c < vec_per_row; c += 32) d[c] = __ldg(s + c);
+    const uint4* sp = src + (size_t)t * vec_per_row;
+    uint4 v[kDispatchNV];
+#pragma unroll
+    for (int i = 0; i < kDispatchNV; ++i) {
+      const int c = c0 + i * 32 + lane;
+      if (c < vec_per_row) v[i] = __ldg(sp + c);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int r = __shfl_sync(0xffffffffu, my, j);
+      if (r < 0) continue;
+      uint4* d = dst + (size_t)r * vec_per_row;
+#pragma unroll
+      for (int i = 0; i < kDispatchNV; ++i) {
+        const int c = c0 + i * 32 + lane;
+        if (c < vec_per_row) d[c] = v[i];
+      }
+    }
+  }
+  // pad rows, and rows whose assignment index is out of range, are zero:
+  // each lane tests one row, the warp clears the flagged rows together
+  for (int64_t rb = (int64_t)global_warp() * 32; rb < rows; rb += (int64_t)grid_warps() * 32) {
+    const int64_t r = rb + lane;
+    const int a = r < rows ? assign_of_row[r] : 0;
+    if (r < rows && a >= n_assign) report(status, MOE_ERR_BAD_INDEX);
+    unsigned m = __ballot_sync(0xffffffffu, r < rows && (a < 0 || a >= n_assign));
+    while (m) {
+      const int i = __ffs(m) - 1;
+      m &= m - 1;
+      uint4* d = dst + (size_t)(rb + i) * vec_per_row;
+      for (int c = lane; c < vec_per_row; c += 32) d[c] = make_uint4(0, 0, 0, 0);
+    }
   }
 }
 
@@ -192,11 +232,15 @@ int grid_for_rows(int64_t rows) {
 
 cudaError_t launch_gather_rows(const void* src, void* dst, int H, int elem_bytes, int k,
                                int n_assign, const int32_t* assign_of_row,
-                               const int32_t* padded_offsets, int E, int64_t max_rows,
-                               int32_t* status, cudaStream_t s) {
+                               const int32_t* row_of_assign, const int32_t* padded_offsets,
+                               int E, int64_t max_rows, int32_t* status, cudaStream_t s) {
   const int vec = H * elem_bytes / 16;
-  gather_rows_kernel<<<grid_for_rows(max_rows), kThreads, 0, s>>>(
-      (const uint4*)src, (uint4*)dst, vec, k, n_assign, assign_of_row, padded_offsets, E, status);
+  const int T = n_assign / k;
+  const int nch = (vec + 32 * kDispatchNV - 1) / (32 * kDispatchNV);
+  const int64_t units = (int64_t)T * nch;
+  dispatch_rows_kernel<<<grid_for_rows(units > max_rows / 32 ? units : max_rows / 32), kThreads, 0,
+                         s>>>((const uint4*)src, (uint4*)dst, vec, T, k, n_assign, row_of_assign,
+                              assign_of_row, padded_offsets, E, status);
   return cudaGetLastError();
 }
 

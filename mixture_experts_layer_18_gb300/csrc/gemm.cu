@@ -658,6 +658,16 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
     auto spare_col = [&](int c) {
       return tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(C::SPARE_COL + h * 64 + c);
     };
+    // gate of a tile row: 1 without a gate vector, 0 on pad rows
+    auto row_gate = [&](const GemmProblem& gp, int row) -> float {
+      if (!gp.gate) return 1.f;
+      int a = gp.assign_of_row[row];
+      if (a >= gp.n_assign) {           // corrupted map: treat as a pad row
+        report(P.status, MOE_ERR_BAD_INDEX);
+        a = -1;
+      }
+      return a >= 0 ? gp.gate[a] : 0.f;
+    };
     auto release_now = [&]() {
       tc_fence_before();
       __syncwarp();
@@ -671,15 +681,7 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       // and bulk stores run while the next tile's MMAs do.
       if (ti.kind == GK_FWD2 || ti.kind == GK_BWD_DX || ti.kind == GK_DW) {
         const bool have = ti.valid && !(ti.kind == GK_DW && ti.nk == 0);   // CTA-uniform
-        float gt = 1.f;
-        if (ti.kind == GK_FWD2 && ti.valid) {
-          int a = g.assign_of_row[ti.m0 + r];
-          if (a >= g.n_assign) {          // corrupted map: treat as a pad row
-            report(P.status, MOE_ERR_BAD_INDEX);
-            a = -1;
-          }
-          gt = a >= 0 ? g.gate[a] : 0.f;
-        }
+        const float gt = ti.kind == GK_FWD2 && ti.valid ? row_gate(g, ti.m0 + r) : 1.f;
         uint32_t pk[64];
         if (have) {
           tmem_ld64(taddr + cb, x);
@@ -734,6 +736,9 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       const int row = ti.m0 + r;
       Elt* outA = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
       Elt* h13 = g.out2 ? static_cast<Elt*>(g.out2) + (size_t)row * g.ld_out2 + ti.n0 : nullptr;
+      // with a gate vector the activation leaves as gate * A (0 on pad rows)
+      const float ga = row_gate(g, row);
+      const bool zrow = ga == 0.f;
       const int half = cb + cw / 2;
       if constexpr (C::SPLIT) tmem_move32x2(taddr + half, taddr + C::BN / 2 + half, spare_col(0));
 #pragma unroll 1
@@ -760,7 +765,7 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
           }
         }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = silu_f(v[i]) * w[i];
+        for (int i = 0; i < 32; ++i) v[i] = zrow ? 0.f : silu_f(v[i]) * w[i] * ga;
         if constexpr (TS) {
           stage_begin();
           stage_bf16_row(sb0, lane, v);
@@ -775,12 +780,7 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       }
     } else if (ti.kind == GK_FWD2) {
       const int row = ti.m0 + r;
-      int a = g.assign_of_row[row];
-      if (a >= g.n_assign) {          // corrupted map: treat as a pad row
-        report(P.status, MOE_ERR_BAD_INDEX);
-        a = -1;
-      }
-      const float gt = a >= 0 ? g.gate[a] : 0.f;
+      const float gt = row_gate(g, row);
       Elt* out = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
 #pragma unroll 1
       for (int c = cb; c < cb + cw; c += 64) {

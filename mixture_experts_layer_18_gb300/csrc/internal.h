@@ -29,8 +29,8 @@ cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int64_t
 // gather.cu  (elem_bytes 4: fp32 storage, 2: bf16 storage)
 cudaError_t launch_gather_rows(const void* src, void* dst, int H, int elem_bytes, int k,
                                int n_assign, const int32_t* assign_of_row,
-                               const int32_t* padded_offsets, int E, int64_t max_rows,
-                               int32_t* status, cudaStream_t s);
+                               const int32_t* row_of_assign, const int32_t* padded_offsets,
+                               int E, int64_t max_rows, int32_t* status, cudaStream_t s);
 cudaError_t launch_gather_grad(const void* dY, void* dY_perm, void* dYg_perm, int H,
                                int elem_bytes, int k, int n_assign, const int32_t* assign_of_row,
                                const float* gate, const int32_t* padded_offsets, int E,

@@ -85,6 +85,11 @@ int bn_bwd(const moe_dims* d) {
   return 0;
 }
 
+// bf16 mode applies the gate to A in the gate/up epilogue (the saved `act`
+// is gate * A): the down GEMM then needs no gate, and dW2 = (gate * A)^T
+// dY_perm needs no gated copy of dY.
+bool gate_on_act(const moe_dims* d) { return d->mode == MOE_BF16; }
+
 // fp32 mode keeps every TF32 operand K-major: the weight operands and the
 // token-axis operands of the weight-gradient GEMMs get transposed copies whose
 // row pitch is the row capacity rounded up to 32.
@@ -142,8 +147,10 @@ BwdWs bwd_ws(const moe_dims* d) {
   const int bn = bn_bwd(d);
   w.nt_d = bn ? d->I / bn : 1;
   size_t o = 0;
-  w.dy_perm = o; o += align256(rows * d->H * es);
-  w.dyg_perm = o; o += align256(rows * d->H * es);
+  // dY_perm (bf16, f32) and gate * dY_perm (f32); the MXFP8 backward
+  // gathers dY straight into its encodings
+  w.dy_perm = o; o += mx_bwd(d) ? 0 : align256(rows * d->H * es);
+  w.dyg_perm = o; o += mx_bwd(d) || gate_on_act(d) ? 0 : align256(rows * d->H * es);
   w.dh13 = o; o += align256(rows * 2 * d->I * es);
   w.dxp = o; o += align256(rows * d->H * es);
   w.partial = o; o += align256(rows * w.nt_d * sizeof(float));
@@ -191,7 +198,8 @@ moe_saved_layout saved_layout(const moe_dims* d) {
   memset(&s, 0, sizeof(s));
   const size_t rows = (size_t)max_rows(d), es = elem_bytes(d);
   size_t o = 0;
-  s.x_perm = o; o += align256(rows * d->H * es);
+  // the MXFP8 forward gathers X straight into its encodings (x_col below)
+  s.x_perm = o; o += d->mode == MOE_MXFP8 ? 0 : align256(rows * d->H * es);
   s.h13 = o; o += align256(rows * 2 * d->I * es);
   s.act = o; o += align256(rows * d->I * es);
   if (d->mode == MOE_MXFP8) {
@@ -546,7 +554,7 @@ moe_status moe_forward(const moe_dims* d, const void* X, const void* W13, const 
     w2_src = w2t;
   }
   MOE_TRY(launch_gather_rows(X, x_perm, d->H, es, d->top_k, n_assign, r->assign_of_row,
-                             r->padded_offsets, d->E, rows, dev_status, s));
+                             r->row_of_assign, r->padded_offsets, d->E, rows, dev_status, s));
   moe_status st;
   EventScope timing(MOE_WS_FORWARD, s);
   EngineLaunch L;
@@ -564,6 +572,9 @@ moe_status moe_forward(const moe_dims* d, const void* X, const void* W13, const 
     g = GemmDesc{};
     g.kind = GK_FWD1;
     g.a = x_perm; g.a_rows = rows; g.a_cols = d->H;
+    if (gate_on_act(d)) {   // A leaves as gate * A (0 on pad rows)
+      g.gate = r->gate; g.assign_of_row = r->assign_of_row; g.n_assign = n_assign;
+    }
     if (f32) {   // W13^T [E*2I, H], K-major
       g.b = w13_src; g.b_rows = (int64_t)d->E * 2 * d->I; g.b_cols = d->H;
       g.b_expert_rows = 2 * d->I;
@@ -594,7 +605,9 @@ moe_status moe_forward(const moe_dims* d, const void* X, const void* W13, const 
     }
     g.N = d->H; g.K = d->I;
     g.out = zg; g.ld_out = d->H;
-    g.gate = r->gate; g.assign_of_row = r->assign_of_row; g.n_assign = n_assign;
+    if (!gate_on_act(d)) {  // Z = gate * (A W2)
+      g.gate = r->gate; g.assign_of_row = r->assign_of_row; g.n_assign = n_assign;
+    }
     MOE_TRY(launch_engine(L, s, &st));
     if (st != MOE_OK) return st;
   }
@@ -646,9 +659,13 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
                                 dev_status, s));
     return MOE_OK;
   }
-  MOE_TRY(launch_gather_grad(dY, dy_perm, dyg_perm, d->H, es, d->top_k, n_assign,
-                             r->assign_of_row, r->gate, r->padded_offsets, d->E, rows, dev_status,
-                             s));
+  if (gate_on_act(d))   // the forward left gate * A in `act`: dY_perm alone
+    MOE_TRY(launch_gather_rows(dY, dy_perm, d->H, es, d->top_k, n_assign, r->assign_of_row,
+                               r->row_of_assign, r->padded_offsets, d->E, rows, dev_status, s));
+  else
+    MOE_TRY(launch_gather_grad(dY, dy_perm, dyg_perm, d->H, es, d->top_k, n_assign,
+                               r->assign_of_row, r->gate, r->padded_offsets, d->E, rows,
+                               dev_status, s));
   MOE_TRY(cudaMemsetAsync(ready, 0, ((rows + 127) / 128 + 1) * sizeof(int32_t), s));
   const bool f32 = d->mode == MOE_F32;
   const int64_t lt = ld_t(d);
@@ -703,7 +720,8 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
   if (!f32) {
     gw2.a_mn = gw2.b_mn = 1;
     gw2.a = act; gw2.a_rows = rows; gw2.a_cols = d->I;
-    gw2.b = dyg_perm; gw2.b_rows = rows; gw2.b_cols = d->H;
+    // dW2 = (gate * A)^T dY_perm (bf16: `act` holds gate * A)
+    gw2.b = gate_on_act(d) ? dy_perm : dyg_perm; gw2.b_rows = rows; gw2.b_cols = d->H;
     gx.dep = DEP_MBLOCK;
     gw13.dep = DEP_EXPERT;
     gw13.a_mn = gw13.b_mn = 1;

@@ -69,7 +69,15 @@ class MoELayer:
 
     @property
     def x_perm(self):
+        """Gathered tokens [rows, H]; None in mxfp8 mode (not stored)."""
+        if self.mode == "mxfp8":
+            return None
         return self._view(self.layout.x_perm, self.max_rows, self.H)
+
+    @property
+    def act_is_gated(self):
+        """bf16 mode stores gate * A in `act` (see moe.h)."""
+        return self.mode == "bf16"
 
     @property
     def h13(self):

@@ -43,8 +43,13 @@ def test_sizes_follow_the_documented_layout():
     assert lay.h13 >= rows * 4096 * 2 and lay.act >= lay.h13 + rows * 3072 * 2
     assert lay.total >= lay.act + rows * 1536 * 2
     assert M.moe_workspace_size(d, M.MOE_WS_FORWARD) >= rows * 4096 * 2
-    assert M.moe_workspace_size(d, M.MOE_WS_BACKWARD) >= rows * (3 * 4096 + 3072) * 2
+    # dY_perm, dh13, dXp (bf16 saves gate * A, so no gated copy of dY)
+    assert M.moe_workspace_size(d, M.MOE_WS_BACKWARD) >= rows * (2 * 4096 + 3072) * 2
     assert M.moe_workspace_size(d, 99) == 0
+    # MXFP8: no X_perm (the dispatch gather writes MXFP8 encodings directly)
+    lay8 = M.moe_saved_layout_of(_dims(T=16384, H=4096, E=128, I=1536, top_k=8,
+                                       mode=M.MOE_MXFP8))
+    assert lay8.x_perm == 0 and lay8.h13 == 0
 
 
 def test_null_and_misaligned_pointers_rejected_on_host():

@@ -44,17 +44,22 @@ def _check_small(cfg, seed=0, mode=None, tol=TOL_BF16):
     idx, gate = O.route(inp["logits"], cfg.k)
     Y, saved = O.forward(oi["X"], oi["W13"], oi["W2"], idx, gate, keep=True)
     g = O.backward(oi["X"], oi["W13"], oi["W2"], idx, gate, oi["dY"])
-    # intermediates: gathered rows, h13 and the activation, row by row
+    # intermediates: gathered rows, h13 and the activation (gate * A in bf16
+    # mode), row by row
     roa = L.row_of_assign.cpu().numpy()
     xp, h13, act = to_f64(L.x_perm), to_f64(L.h13), to_f64(L.act)
     X = np.asarray(oi["X"], np.float64)
+    g_of_a = np.asarray(gate, np.float64).reshape(-1)
     for e, s in saved.items():
         rows = roa[s["a"]]
         assert np.array_equal(xp[rows], X[s["a"] // cfg.k]), e
         assert rel_err(h13[rows], s["h"]) <= tol, ("h13", e)
-        assert rel_err(act[rows], s["A"]) <= tol, ("act", e)
+        A = s["A"] * g_of_a[s["a"]][:, None] if L.act_is_gated else s["A"]
+        assert rel_err(act[rows], A) <= tol, ("act", e)
     pad = L.assign_of_row.cpu().numpy()[: int(L.padded_offsets[-1])] < 0
     assert (xp[: len(pad)][pad] == 0).all()
+    if L.act_is_gated:
+        assert (act[: len(pad)][pad] == 0).all()
     errs = {"Y": rel_err(to_f64(io["Y"]), Y), "dX": rel_err(to_f64(io["dX"]), g["dX"]),
             "dW13": rel_err(to_f64(io["dW13"]), g["dW13"]),
             "dW2": rel_err(to_f64(io["dW2"]), g["dW2"]),
