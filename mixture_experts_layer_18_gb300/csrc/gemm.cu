@@ -743,11 +743,12 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       if constexpr (C::SPLIT) tmem_move32x2(taddr + half, taddr + C::BN / 2 + half, spare_col(0));
 #pragma unroll 1
       for (int c = cb; c < cb + cw; c += 32) {
-        if (C::SPLIT && c == half) release_now();
         if (C::SPLIT && c >= half)
           tmem_ld32x2(spare_col(c - half), spare_col(c - half + 32), v, w);
         else
           tmem_ld32x2(taddr + c, taddr + C::BN / 2 + c, v, w);   // u: gate half, v: up half
+        // the last accumulator chunk is in registers: release before its stores
+        if (C::SPLIT && c + 32 == half) release_now();
         if (h13) {
           if constexpr (TS) {
             stage_begin();
@@ -805,9 +806,13 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
 #pragma unroll 1
       for (int c = cb; c < cb + cw; c += 32, src += 32) {
         float D[32];
-        if (C::SPLIT && c == half) {
-          release_now();
-          src = spare_col(0);
+        if constexpr (C::SPLIT) {
+          // D first: the last accumulator chunk is in registers, release
+          // before its math (this order also keeps the pair under its
+          // register cap)
+          if (c == half) src = spare_col(0);
+          tmem_ld32(src, D);
+          if (c + 32 == half) release_now();
         }
         unpack_raw<Elt, NV>(pu, v);            // u of this chunk
         unpack_raw<Elt, NV>(pv, w);            // v of this chunk
@@ -815,7 +820,7 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
           load_raw<Elt, NV>(h13a + c + 32, pu);
           load_raw<Elt, NV>(h13a + g.I + c + 32, pv);
         }
-        tmem_ld32(src, D);
+        if constexpr (!C::SPLIT) tmem_ld32(src, D);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float u = v[i], vv = w[i];
