@@ -109,7 +109,10 @@ typedef struct {
  *   h13    [rows, 2I]  X_perm_e W13_e before the activation (if save_for_backward)
  *   act    [rows, I]   A = silu(h13[:, :I]) * h13[:, I:]; in MOE_BF16 mode
  *                      gate * A (the gate of the row's assignment, 0 on pad
- *                      rows), the form both the down GEMM and dW2 consume
+ *                      rows), the form both the down GEMM and dW2 consume;
+ *                      zero-sized in MOE_MXFP8 mode (the gate/up epilogue
+ *                      writes A's MXFP8 encodings directly: act_col below,
+ *                      and a row-wise copy in the forward workspace)
  * MOE_MXFP8 only (zero-sized in the other modes): the backward's MXFP8
  * operands, which the forward quantises in the same passes as its own
  * (E4M3 codes *_q, tensor-core scale atoms *_sf; written only with

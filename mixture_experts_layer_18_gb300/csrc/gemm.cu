@@ -19,8 +19,10 @@
 //   FWD1   h13 = X_perm_e W13_e, epilogue A = silu(u) * v (+ store h13)
 //          A: X_perm [rows, H] K-major;  B: W13 as [E*H, 2I] N-major.
 //          One MMA tile of N = BN covers BN/2 gate columns and the same BN/2
-//          up columns, so the activation needs no second pass.
-//   FWD2   Z = gate * (A_e W2_e)
+//          up columns, so the activation needs no second pass.  With a gate
+//          vector (bf16) A leaves as gate * A; block-scaled runs write A's
+//          MXFP8 encodings instead of bf16.
+//   FWD2   Z = gate * (A_e W2_e)  (no gate when FWD1 applied it)
 //          A: act [rows, I] K-major;  B: W2 as [E*I, H] N-major.
 //   BWD_D  D = dY_perm_e W2_e^T, epilogue dSwiGLU -> dh13, d(gate) partials
 //          A: dY_perm [rows, H] K-major;  B: W2 as [E*I, H] K-major.
@@ -50,6 +52,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "mx_encode.cuh"
 
 namespace moe {
 
@@ -75,6 +78,14 @@ struct GemmProblem {
   const int32_t* assign_of_row;
   int n_assign;      // valid assignment indices are [0, n_assign)
   float* partial;
+  // FWD1 of a block-scaled run: A leaves as its MXFP8 encodings instead of
+  // bf16 (codes [rows, I] and tensor-core scale atoms; row-wise blocks along
+  // I, and column-wise blocks of 32 rows when enc_col_q is set)
+  uint8_t* enc_row_q;
+  uint8_t* enc_row_sf;
+  uint8_t* enc_col_q;
+  uint8_t* enc_col_sf;
+  int64_t enc_col_kg;  // 128-row groups of the column-wise scale atoms
   // MXFP8 operands: E8M0 scale atoms (512 B per 128 MN indices x 128 K),
   // read through [atoms * 4, 128]-byte views: atom i is rows 4i .. 4i + 3.
   CUtensorMap tmSFA;
@@ -473,6 +484,51 @@ __device__ void mma_role(const EngineParams& P, const int* cum, int total, const
 }
 
 // ------------------------------------------------------- epilogue helpers
+// MXFP8 encodings of a warp's 32 x 32 block of A (lane = row, v = its 32
+// columns from col0), from the bf16 values the stored A would hold, so the
+// codes equal those of the quantiser kernels on the stored tensor:
+// row-wise (one 32-column block per lane) and, when qc is set, column-wise
+// (one 32-row block per column: the warp's rows lie in one expert's group,
+// whose padded start is a multiple of 128).
+__device__ __forceinline__ void encode_mx_block(float (&v)[32], int64_t row, int col0, int C,
+                                                uint8_t* qr, uint8_t* sr, uint8_t* qc,
+                                                uint8_t* sc, int64_t kg_rows, int lane) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+  float am = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(v[i]));
+  const int sb = mx_scale_byte(am);
+  const float inv = mx_inv_scale(sb);
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    o[i] = (uint32_t)e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv) |
+           ((uint32_t)e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv) << 16);
+  uint4* dr = reinterpret_cast<uint4*>(qr + (size_t)row * C + col0);
+  dr[0] = make_uint4(o[0], o[1], o[2], o[3]);
+  dr[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  sr[mma_scale_index(row, col0 >> 5, C >> 7)] = (uint8_t)sb;
+  if (!qc) return;
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    float m0 = fabsf(v[i]), m1 = fabsf(v[i + 1]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, off));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, off));
+    }
+    const int s0 = mx_scale_byte(m0), s1 = mx_scale_byte(m1);
+    const uint32_t c2 = e4m3x2(v[i] * mx_inv_scale(s0), v[i + 1] * mx_inv_scale(s1));
+    if (i & 2) o[i >> 2] |= c2 << 16; else o[i >> 2] = c2;
+    if (lane == i) sc[mma_scale_index(col0 + i, (int)(row >> 5), kg_rows)] = (uint8_t)s0;
+    if (lane == i + 1) sc[mma_scale_index(col0 + i + 1, (int)(row >> 5), kg_rows)] = (uint8_t)s1;
+  }
+  uint4* dc = reinterpret_cast<uint4*>(qc + (size_t)row * C + col0);
+  dc[0] = make_uint4(o[0], o[1], o[2], o[3]);
+  dc[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 template <typename Elt>
 __device__ __forceinline__ void store32(Elt* dst, const float (&v)[32]) {
   uint4* d = reinterpret_cast<uint4*>(dst);
@@ -767,7 +823,10 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
         }
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = zrow ? 0.f : silu_f(v[i]) * w[i] * ga;
-        if constexpr (TS) {
+        if (C::MX && g.enc_row_q) {
+          encode_mx_block(v, row, ti.n0 + c, g.I, g.enc_row_q, g.enc_row_sf, g.enc_col_q,
+                          g.enc_col_sf, g.enc_col_kg, lane);
+        } else if constexpr (TS) {
           stage_begin();
           stage_bf16_row(sb0, lane, v);
           stage_end();
@@ -1214,6 +1273,11 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
     g.partial = d.partial;
     g.sfa_kg = d.sfa_kg;
     g.sfb_kg = d.sfb_kg;
+    g.enc_row_q = d.enc_row_q;
+    g.enc_row_sf = d.enc_row_sf;
+    g.enc_col_q = d.enc_col_q;
+    g.enc_col_sf = d.enc_col_sf;
+    g.enc_col_kg = d.enc_col_kg;
     if (es == 1 && !(make_tmap_sf(&g.tmSFA, d.sfa, d.sfa_bytes) &&
                      make_tmap_sf(&g.tmSFB, d.sfb, d.sfb_bytes))) {
       *st = MOE_ERR_INVALID_ARG;
@@ -1232,12 +1296,18 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
     ok = ok && (b_mn ? make_tmap(&g.tmB, d.b, es, d.b_rows, d.b_cols, ATOM, BK)
                      : make_tmap(&g.tmB, d.b, es, d.b_rows, d.b_cols, BK,
                                  d.kind == GK_FWD1 ? L.BN / 2 : L.BN / pair));
-    if (es != 4 && d.out) {   // bf16 results: bulk-store views of the outputs
+    if (es != 4) {   // bf16 results: bulk-store views of the outputs
+      // every bf16 result leaves through a view built here; the one result
+      // that may be absent is FWD1's A when the epilogue encodes it instead
+      if (!d.out && !(d.kind == GK_FWD1 && d.enc_row_q)) {
+        *st = MOE_ERR_INVALID_ARG;
+        return cudaSuccess;
+      }
       if (d.kind == GK_DW) {
         if (d.ld_out != d.N) { *st = MOE_ERR_UNSUPPORTED; return cudaSuccess; }
         ok = make_tmap_out3(&g.tmO, d.out, L.E, d.M, d.N);
       } else {
-        ok = make_tmap_out(&g.tmO, d.out, L.max_rows, d.ld_out);
+        if (d.out) ok = make_tmap_out(&g.tmO, d.out, L.max_rows, d.ld_out);
         if (ok && d.out2) ok = make_tmap_out(&g.tmO2, d.out2, L.max_rows, d.ld_out2);
       }
     }

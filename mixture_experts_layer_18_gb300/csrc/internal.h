@@ -92,6 +92,11 @@ struct GemmDesc {
   const int32_t* assign_of_row;
   int n_assign;
   float* partial;
+  uint8_t* enc_row_q;          // FWD1, MXFP8: A's encodings written by the epilogue
+  uint8_t* enc_row_sf;         //   (row-wise; column-wise when enc_col_q is set)
+  uint8_t* enc_col_q;
+  uint8_t* enc_col_sf;
+  int64_t enc_col_kg;          //   128-row groups of the column-wise scale atoms
   const uint8_t* sfa;          // MXFP8: scale atoms of A / B (quant.cu layout 1)
   const uint8_t* sfb;
   int64_t sfa_bytes, sfb_bytes;  // size of each scale-atom array (multiple of 512)

@@ -201,7 +201,9 @@ moe_saved_layout saved_layout(const moe_dims* d) {
   // the MXFP8 forward gathers X straight into its encodings (x_col below)
   s.x_perm = o; o += d->mode == MOE_MXFP8 ? 0 : align256(rows * d->H * es);
   s.h13 = o; o += align256(rows * 2 * d->I * es);
-  s.act = o; o += align256(rows * d->I * es);
+  // MXFP8 keeps A only as its encodings (x_col / act_col below, and the
+  // forward workspace's row-wise copy)
+  s.act = o; o += d->mode == MOE_MXFP8 ? 0 : align256(rows * d->I * es);
   if (d->mode == MOE_MXFP8) {
     const size_t rp = (size_t)rows_pad(d), EH = (size_t)d->E * d->H, EI = (size_t)d->E * d->I;
     const MxBuf x = mx_carve(o, rows, rp, d->H), a = mx_carve(o, rows, rp, d->I);
@@ -280,9 +282,11 @@ MxSaved mx_saved(const moe_dims* d, const moe_saved_layout& sl, char* sv) {
 // With save_for_backward, each quantisation pass also writes the backward's
 // encoding of the same tensor into `saved` (one read, both layouts).
 // The dispatch gather is fused into the first quantisation: X_perm exists
-// only as its MXFP8 encodings (saved x_perm is not written in this mode).
+// only as its MXFP8 encodings (saved x_perm is not stored in this mode); the
+// gate/up epilogue writes A's two encodings itself (A is never stored in
+// bf16 in this mode).
 moe_status forward_mx(const moe_dims* d, const void* X, const void* W13, const void* W2,
-                      const moe_route_out* r, void* h13, void* act, void* zg, char* wsb,
+                      const moe_route_out* r, void* h13, void* zg, char* wsb,
                       const FwdWs& w, const MxSaved& sv, int32_t* dev_status, cudaStream_t s) {
   const int64_t rows = max_rows(d), rp = rows_pad(d);
   const int H = d->H, I = d->I, E = d->E;
@@ -316,16 +320,20 @@ moe_status forward_mx(const moe_dims* d, const void* X, const void* W13, const v
     g.b = w13.q; g.b_rows = (int64_t)E * H; g.b_cols = 2 * I; g.b_expert_rows = H;
     g.sfb = w13.sf; g.sfb_bytes = w13.sf_bytes; g.sfb_kg = (int)((int64_t)E * H / 128);
     g.N = 2 * I; g.K = H; g.I = I;
-    g.out = act; g.ld_out = I;
+    // A leaves the epilogue as its MXFP8 encodings (row-wise for the down
+    // GEMM, column-wise along tokens for dW2), never as bf16
+    g.enc_row_q = (uint8_t*)a.q; g.enc_row_sf = (uint8_t*)a.sf;
+    if (both) {
+      g.enc_col_q = (uint8_t*)sv.act_col.q; g.enc_col_sf = (uint8_t*)sv.act_col.sf;
+      g.enc_col_kg = rp / 128;
+    }
     g.out2 = d->save_for_backward ? h13 : nullptr; g.ld_out2 = 2 * I;
     MOE_TRY(launch_engine(L, s, &st));
     if (st != MOE_OK) return st;
   }
   if (both) {
-    MOE_TRY(quant_both(act, rows, I, tpad, a, &sv.act_col, s));
     MOE_TRY(quant_both(W2, (int64_t)E * I, H, nullptr, sv.w2_row, &w2, s));
   } else {
-    MOE_TRY(quant_rows(act, rows, I, a, dev_status, s));
     MOE_TRY(quant_cols(W2, (int64_t)E * I, H, nullptr, 0, w2, dev_status, s));
   }
   {
@@ -342,7 +350,6 @@ moe_status forward_mx(const moe_dims* d, const void* X, const void* W13, const v
     MOE_TRY(launch_engine(L, s, &st));
     if (st != MOE_OK) return st;
   }
-  (void)rp;
   return MOE_OK;
 }
 
@@ -535,7 +542,7 @@ moe_status moe_forward(const moe_dims* d, const void* X, const void* W13, const 
 
   if (mx_fwd(d)) {
     EventScope timing(MOE_WS_FORWARD, s);
-    const moe_status st = forward_mx(d, X, W13, W2, r, h13, act, zg, static_cast<char*>(ws), w,
+    const moe_status st = forward_mx(d, X, W13, W2, r, h13, zg, static_cast<char*>(ws), w,
                                      mx_saved(d, sl, sv), dev_status, s);
     if (st != MOE_OK) return st;
     timing.finish();

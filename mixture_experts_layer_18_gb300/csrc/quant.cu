@@ -18,35 +18,11 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "mx_encode.cuh"
 
 namespace moe {
 
 namespace {
-
-__device__ __forceinline__ int mx_scale_byte(float amax) {
-  const int f = (__float_as_uint(amax) >> 23) & 0xFF;
-  return f > 8 ? f - 8 : 0;
-}
-
-// 2^-s as fp32 for a scale byte b (s = b - 127, so 2^-s = 2^(127 - b)).
-__device__ __forceinline__ float mx_inv_scale(int b) {
-  return __uint_as_float((uint32_t)(254 - b) << 23);
-}
-
-// Byte index of the scale of (MN index mn, 32-element K block kb) in the
-// tensor-core scale-factor layout: 512-byte atoms cover 128 MN indices x 4 K
-// blocks, atom (mn/128, kb/4) at (mn/128) * kgroups + kb/4, and inside an atom
-// byte (mn % 32) * 16 + ((mn / 32) % 4) * 4 + kb % 4.  Copied to tensor memory
-// with tcgen05.cp (32x128b, replicated to the four lane quarters), row mn
-// reads lane mn, column mn / 32, byte kb % 4.
-__device__ __forceinline__ size_t mma_scale_index(int64_t mn, int kb, int64_t kgroups) {
-  return ((size_t)(mn >> 7) * kgroups + (kb >> 2)) * 512 + (size_t)(mn & 31) * 16 +
-         (size_t)((mn >> 5) & 3) * 4 + (kb & 3);
-}
-
-__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
-  return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
-}
 
 // axis 1: one thread per 32-element block of a row (64 contiguous bytes in,
 // 32 bytes of codes + 1 scale byte out).

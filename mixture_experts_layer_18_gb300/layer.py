@@ -85,6 +85,10 @@ class MoELayer:
 
     @property
     def act(self):
+        """The activation [rows, I] (gate * A in bf16 mode); None in mxfp8
+        mode, which keeps A only as its MXFP8 encodings."""
+        if self.mode == "mxfp8":
+            return None
         return self._view(self.layout.act, self.max_rows, self.I)
 
     def device_status(self) -> int:

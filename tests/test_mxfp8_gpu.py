@@ -130,6 +130,41 @@ def test_saved_encodings_bit_exact():
         assert np.array_equal(sv[off_s + atom_byte(r, kb, C // 128)], rs), name
 
 
+def test_activation_encodings_from_the_epilogue():
+    """In mxfp8 mode the gate/up epilogue writes A's MXFP8 encodings itself
+    (A is never stored in bf16).  Its column-wise encoding in `saved` (the
+    dW2 operand: 32-row blocks per expert group) decodes to the oracle's A
+    within the MXFP8 tolerance, and nearly all of its codes and scale bytes
+    equal the oracle quantiser's on the oracle's bf16-rounded A (a wrong
+    row, column, block or atom index would leave few equal; the rest differ
+    where fp32 and fp64 sums round A to different bf16 values)."""
+    cfg = SMALL[1]
+    inp = make_inputs(cfg, 7)
+    L, _ = _run(cfg, inp, "mxfp8")
+    assert L.act is None
+    lay, sv = L.layout, L.saved.cpu().numpy()
+    rows = L.max_rows
+    rp = (rows + 127) // 128 * 128
+    I = cfg.I
+    oi = _oracle_inputs(inp)
+    idx, gate = O.route(inp["logits"], cfg.k)
+    _, saved = O.forward(oi["X"], oi["W13"], oi["W2"], idx, gate, mode="mxfp8", keep=True)
+    pm = O.permute(idx, cfg.E)
+    tpad = int(pm["padded_offsets"][-1])
+    A = np.zeros((tpad, I))
+    for e, s in saved.items():
+        A[pm["row_of_assign"][s["a"]]] = s["A"]
+    cq, cs = O.quantize_mxfp8(O.bf16_round(A), 0, pm["padded_offsets"])
+    q = sv[lay.act_col_q: lay.act_col_q + rows * I].reshape(rows, I)[:tpad]
+    rb, c = np.meshgrid(np.arange(tpad // 32), np.arange(I), indexing="ij")
+    sf = sv[lay.act_col_sf + atom_byte(c, rb, rp // 128)]
+    assert (q == cq).mean() >= 0.95, (q == cq).mean()
+    assert (sf == cs).mean() >= 0.98, (sf == cs).mean()
+    # element error of the MX rule: at most 1/8 of the block maximum (values
+    # past 448 * 2^s saturate: s = floor(log2(amax)) - 8), plus bf16 rounding
+    assert rel_err(O.dequantize_mxfp8(q, sf, 0), A) <= 0.13
+
+
 @pytest.mark.parametrize("mode", ["mxfp8", "fp8_bwd"])
 def test_full_size_235b_sampled(mode):
     """235B layer shape.  The oracle is run on k=1 sub-batches: Y, dX and
