@@ -489,10 +489,14 @@ __device__ void mma_role(const EngineParams& P, const int* cum, int total, const
 // codes equal those of the quantiser kernels on the stored tensor:
 // row-wise (one 32-column block per lane) and, when qc is set, column-wise
 // (one 32-row block per column: the warp's rows lie in one expert's group,
-// whose padded start is a multiple of 128).
+// whose padded start is a multiple of 128).  The column maxima go through
+// `tsm`, 4 KB of this warp's shared memory that no copy is reading: lane r
+// writes |v[i]| to word 32 r + (i ^ r), lane j reads column j (both without
+// bank conflicts), and the per-column factors return by shuffle.
 __device__ __forceinline__ void encode_mx_block(float (&v)[32], int64_t row, int col0, int C,
                                                 uint8_t* qr, uint8_t* sr, uint8_t* qc,
-                                                uint8_t* sc, int64_t kg_rows, int lane) {
+                                                uint8_t* sc, int64_t kg_rows, float* tsm,
+                                                int lane) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
   float am = 0.f;
@@ -511,18 +515,20 @@ __device__ __forceinline__ void encode_mx_block(float (&v)[32], int64_t row, int
   sr[mma_scale_index(row, col0 >> 5, C >> 7)] = (uint8_t)sb;
   if (!qc) return;
 #pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    float m0 = fabsf(v[i]), m1 = fabsf(v[i + 1]);
+  for (int i = 0; i < 32; ++i) tsm[lane * 32 + (i ^ lane)] = fabsf(v[i]);
+  __syncwarp();
+  float cm = 0.f;                      // maximum of column `lane`
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, off));
-      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, off));
-    }
-    const int s0 = mx_scale_byte(m0), s1 = mx_scale_byte(m1);
-    const uint32_t c2 = e4m3x2(v[i] * mx_inv_scale(s0), v[i + 1] * mx_inv_scale(s1));
+  for (int r = 0; r < 32; ++r) cm = fmaxf(cm, tsm[r * 32 + (lane ^ r)]);
+  __syncwarp();                        // reads done before the staging is reused
+  const int sj = mx_scale_byte(cm);
+  sc[mma_scale_index(col0 + lane, (int)(row >> 5), kg_rows)] = (uint8_t)sj;
+  const float invj = mx_inv_scale(sj);
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const float i0 = __shfl_sync(0xffffffffu, invj, i), i1 = __shfl_sync(0xffffffffu, invj, i + 1);
+    const uint32_t c2 = e4m3x2(v[i] * i0, v[i + 1] * i1);
     if (i & 2) o[i >> 2] |= c2 << 16; else o[i >> 2] = c2;
-    if (lane == i) sc[mma_scale_index(col0 + i, (int)(row >> 5), kg_rows)] = (uint8_t)s0;
-    if (lane == i + 1) sc[mma_scale_index(col0 + i + 1, (int)(row >> 5), kg_rows)] = (uint8_t)s1;
   }
   uint4* dc = reinterpret_cast<uint4*>(qc + (size_t)row * C + col0);
   dc[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -824,8 +830,9 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = zrow ? 0.f : silu_f(v[i]) * w[i] * ga;
         if (C::MX && g.enc_row_q) {
+          if (g.enc_col_q) stage_begin();   // the staging becomes the column-maximum scratch
           encode_mx_block(v, row, ti.n0 + c, g.I, g.enc_row_q, g.enc_row_sf, g.enc_col_q,
-                          g.enc_col_sf, g.enc_col_kg, lane);
+                          g.enc_col_sf, g.enc_col_kg, reinterpret_cast<float*>(sb0), lane);
         } else if constexpr (TS) {
           stage_begin();
           stage_bf16_row(sb0, lane, v);
