@@ -52,6 +52,51 @@ def test_sizes_follow_the_documented_layout():
     assert lay8.x_perm == 0 and lay8.h13 == 0
 
 
+def _span(lay, name, following):
+    """Bytes between a saved-layout field and the next one."""
+    return getattr(lay, following) - getattr(lay, name)
+
+
+@pytest.mark.parametrize("mode, x_perm, act", [
+    ("MOE_BF16", True, True), ("MOE_F32", True, True),
+    ("MOE_FP8_BWD", True, True),       # its MXFP8 backward quantises X_perm and A
+    ("MOE_MXFP8", False, False),       # both exist only as MXFP8 encodings
+])
+def test_saved_tensors_per_mode(mode, x_perm, act):
+    """Which bf16 / fp32 intermediates each mode keeps in `saved` (the
+    MXFP8 forward gathers X into its encodings and encodes A in the SwiGLU
+    epilogue; moe.h documents the zero-sized fields)."""
+    T, H, E, I, k = 1024, 256, 8, 128, 2
+    d = _dims(T=T, H=H, E=E, I=I, top_k=k, mode=getattr(M, mode))
+    rows = T * k + 128 * E
+    es = 4 if mode == "MOE_F32" else 2
+    lay = M.moe_saved_layout_of(d)
+    assert (_span(lay, "x_perm", "h13") >= rows * H * es) == x_perm
+    assert (_span(lay, "x_perm", "h13") == 0) == (not x_perm)
+    assert _span(lay, "h13", "act") >= rows * 2 * I * es
+    nxt = "x_col_q" if mode == "MOE_MXFP8" else "total"
+    assert (_span(lay, "act", nxt) >= rows * I * es) == act
+    if mode == "MOE_MXFP8":
+        rp = (rows + 127) // 128 * 128
+        assert lay.act == lay.x_col_q               # A: no bf16 copy
+        assert lay.act_col_q - lay.x_col_q >= rows * H + rp * H // 32
+        assert lay.total - lay.w2_row_q >= E * I * H + E * I * H // 32
+
+
+def test_backward_workspace_per_mode():
+    """bf16 gathers dY once (the forward left gate * A for dW2); fp32 keeps
+    dY_perm and gate * dY_perm; the MXFP8 modes gather dY into encodings."""
+    T, H, E, I, k = 1024, 256, 8, 128, 2
+    rows = T * k + 128 * E
+    ws = {m: M.moe_workspace_size(_dims(T=T, H=H, E=E, I=I, top_k=k, mode=getattr(M, m)),
+                                  M.MOE_WS_BACKWARD)
+          for m in ("MOE_BF16", "MOE_F32")}
+    # dY_perm + dh13 + dXp (+ partials, counters) in bf16; two dY copies in fp32
+    assert ws["MOE_BF16"] >= rows * (2 * H + 2 * I) * 2
+    assert ws["MOE_BF16"] < rows * (3 * H + 2 * I) * 2
+    assert ws["MOE_F32"] >= rows * (3 * H + 2 * I) * 4
+
+
 def test_null_and_misaligned_pointers_rejected_on_host():
     d = _dims()
     out = M.moe_route_out(*([256] * 7))        # 16-byte aligned but fake; never launched
