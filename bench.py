@@ -26,6 +26,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -63,6 +64,8 @@ def _args():
     p.add_argument("--experts", type=int, default=None, help="override E")
     p.add_argument("--mode", default="bf16", choices=["bf16", "mxfp8", "fp8_bwd"],
                    help="GEMM precision (bf16; MXFP8 forward+backward; bf16 forward + MXFP8 backward)")
+    p.add_argument("--clocks-dir", default=tempfile.gettempdir(),
+                   help="where the raw nvidia-smi clock samples of the timed region are kept")
     p.add_argument("--debug-flags", type=int, default=0,
                    help="library debug flags (diagnosis runs only, e.g. 4 = split backward)")
     return p.parse_args()
@@ -144,10 +147,10 @@ class ClockSampler:
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, directory):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        self.path = os.path.join(directory, f"clocks_bench_{os.getpid()}.csv")
         self.t0 = self.t1 = None   # host wall clock at the start / end of the timed region
 
     def start(self):
@@ -332,7 +335,7 @@ def run_gpu(args):
         a.record()
         b.record()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local, args.clocks_dir)
     clocks.start()
     time.sleep(0.4)
     barrier()
