@@ -80,7 +80,8 @@ __global__ void __launch_bounds__(kThreads) dispatch_rows_kernel(
   }
 }
 
-// dY_perm[r] = dY[t], dYg_perm[r] = gate[a] * dY[t] (t = a / k); pad rows 0.
+// dY_perm[r] = dY[t], dYg_perm[r] = gate[a] * dY[t] (t = a / k); pad rows 0
+// (the fp32 mode's backward; bf16 needs dY_perm alone, from the dispatch).
 template <typename Elt>
 __global__ void __launch_bounds__(kThreads) gather_grad_kernel(
     const uint4* __restrict__ dY, uint4* __restrict__ dYp, uint4* __restrict__ dYgp,

@@ -704,7 +704,8 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
   gd.aux = h13; gd.ld_aux = 2 * d->I;
   gd.gate = r->gate; gd.assign_of_row = r->assign_of_row; gd.n_assign = n_assign;
   gd.partial = partial;
-  // dW2_e = A_e^T (gate * dY)_perm_e   (needs nothing from this launch)
+  // dW2_e = A_e^T (gate * dY)_perm_e = (gate * A)_e^T dY_perm_e, the second
+  // form in bf16 mode (`act` holds gate * A); needs nothing from this launch
   GemmDesc gw2{};
   gw2.kind = GK_DW;
   gw2.M = d->I; gw2.N = d->H;
