@@ -27,7 +27,7 @@ Sources (web pages on the method; cited by title and section):
   [MX]  OCP Microscaling Formats (MX) v1.0: E4M3 elements, 32-element blocks,
         E8M0 shared scale.
 
-Readings taken where the pages are silent (each also listed in the design doc):
+Readings taken where the pages are silent:
   * top-k selects on the logits (same set as on softmax probabilities, since
     exp is monotone); equal logits go to the lower expert index; slot j is the
     j-th largest.  Gates are the softmax over all E renormalised over the k
@@ -68,17 +68,26 @@ def route(logits, k):
 
     Returns ``idx`` int32 [T,k] (slot order: descending logit, ties to the lower
     expert index) and ``gate`` float64 [T,k]: the softmax over all E
-    probabilities of the chosen experts, divided by their sum."""
+    probabilities of the chosen experts, divided by their sum.
+
+    Inputs outside the softmax's domain (readings; the pages only speak of
+    real logits): a NaN logit counts as -inf (never preferred to a number);
+    a token whose logits are all -inf has no softmax and gets gate 0 in every
+    slot, so it contributes nothing to the layer."""
     lg = f64(logits)
+    lg = np.where(np.isnan(lg), -np.inf, lg)
     T, E = lg.shape
     # A stable sort on -logit keeps equal logits in ascending expert order.
     order = np.argsort(-lg, axis=1, kind="stable")
     idx = order[:, :k]
     m = lg.max(axis=1, keepdims=True)
-    p = np.exp(lg - m)
-    p = p / p.sum(axis=1, keepdims=True)            # softmax over all E
-    ps = np.take_along_axis(p, idx, axis=1)
-    gate = ps / ps.sum(axis=1, keepdims=True)       # renormalise over top-k
+    live = np.isfinite(m)                           # False: every logit is -inf
+    p = np.exp(lg - np.where(live, m, 0.0))         # exp(-inf) = 0 on dead rows
+    with np.errstate(invalid="ignore", divide="ignore"):
+        p = p / p.sum(axis=1, keepdims=True)        # softmax over all E
+        ps = np.take_along_axis(p, idx, axis=1)
+        gate = ps / ps.sum(axis=1, keepdims=True)   # renormalise over top-k
+    gate = np.where(live, gate, 0.0)
     return idx.astype(np.int32), gate
 
 
@@ -290,14 +299,31 @@ def _stored(mode, phase):
     return bf16_round if use_mx else f64
 
 
+# Blocked axis of each MXFP8 GEMM operand: the contraction axis of its GEMM
+# ([TE] 03: MXFP8 GEMMs over ragged groups; [MX]: a block is 32 elements
+# along the dot product).  Operands are 2-D: token-major activations have a
+# row per assignment of one expert (1 = along the row, 0 = down the 32-row
+# token blocks of that expert's rows); weights are W13[e] [H, 2I] and
+# W2[e] [I, H] as stored.
+MX_AXES = {
+    # forward:  h = X W13_e (over H),  z = A W2_e (over I)
+    "fwd.X": 1, "fwd.W13": 0, "fwd.A": 1, "fwd.W2": 0,
+    # backward: D = dY W2_e^T (over H),  dX = dh W13_e^T (over 2I)
+    "bwd.dY": 1, "bwd.W2": 1, "bwd.dh_dx": 1, "bwd.W13": 1,
+    # weight gradients over the expert's tokens: dW13_e = X^T dh, dW2_e = A^T (g dY)
+    "bwd.X_dw": 0, "bwd.dh_dw": 0, "bwd.A_dw": 0, "bwd.gdY_dw": 0,
+}
+
+
 def _gemm_operands(mode, phase):
-    """Quantise-dequantise transform applied to GEMM operands: identity for
-    f32/bf16, MXFP8 along the contraction axis for mxfp8 (both phases) and
-    for fp8_bwd (backward only) [MM: fp8_bwd = BF16 forward, FP8 backward]."""
+    """Quantise-dequantise transform applied to a GEMM operand, called as
+    q(x, name) with ``name`` a key of MX_AXES: identity for f32/bf16, MXFP8
+    along MX_AXES[name] for mxfp8 (both phases) and for fp8_bwd (backward
+    only) [MM: fp8_bwd = BF16 forward, FP8 backward]."""
     use_mx = mode == "mxfp8" or (mode == "fp8_bwd" and phase == "bwd")
     if not use_mx:
-        return lambda x, axis: f64(x)
-    return mx_qdq
+        return lambda x, name: f64(x)
+    return lambda x, name: mx_qdq(x, MX_AXES[name])
 
 
 def forward(X, W13, W2, idx, gate, tokens=None, mode="bf16", keep=False):
@@ -326,11 +352,11 @@ def forward(X, W13, W2, idx, gate, tokens=None, mode="bf16", keep=False):
         if a.size == 0:
             continue
         t = a // k
-        x = q(X[t], 1)                                   # rows blocked along H
-        h = x @ q(W13[e], 0)                             # W13_e blocked along H
+        x = q(X[t], "fwd.X")                             # rows blocked along H
+        h = x @ q(W13[e], "fwd.W13")                     # W13_e blocked along H
         u, v = h[:, :I], h[:, I:]
         A = silu(u) * v
-        z = q(st(A), 1) @ q(W2[e], 0)                    # blocked along I
+        z = q(st(A), "fwd.A") @ q(W2[e], "fwd.W2")       # blocked along I
         contrib = g_flat[a][:, None] * z
         for r, tt in enumerate(t):
             Y[pos[int(tt)]] += contrib[r]
@@ -389,20 +415,23 @@ def backward(X, W13, W2, idx, gate, dY, tokens=None, experts=None, mode="bf16"):
         g = g_flat[a][:, None]
         # forward recomputation (the forward's own precision); in the MXFP8
         # backward the saved h and A are the stored (bf16) ones
-        h = qf(X[t], 1) @ qf(W13[e], 0)
+        h = qf(X[t], "fwd.X") @ qf(W13[e], "fwd.W13")
+        # two stored forms of the activation: the forward's own output A
+        # (from the unrounded h, stored once) is the dW2 operand; dSwiGLU and
+        # d(gate) recompute silu(u) * v from the stored pre-activation h
         A_saved = stb((h[:, :I] * sigmoid(h[:, :I])) * h[:, I:])
         h = stb(h)
         u, v = h[:, :I], h[:, I:]
         sg = sigmoid(u)
         A = u * sg * v
         dYt = f64(dY[t])
-        D = qb(dYt, 1) @ qb(W2[e], 1).T                 # contraction over H
+        D = qb(dYt, "bwd.dY") @ qb(W2[e], "bwd.W2").T   # contraction over H
         dA = g * D
         du = dA * v * sg * (1.0 + u * (1.0 - sg))
         dv = dA * (u * sg)
         dh = stb(np.concatenate([du, dv], axis=1))
         dgate_rows = (A * D).sum(axis=1)
-        dx_rows = qb(dh, 1) @ qb(W13[e], 1).T           # contraction over 2I
+        dx_rows = qb(dh, "bwd.dh_dx") @ qb(W13[e], "bwd.W13").T   # contraction over 2I
         for r, (aa, tt) in enumerate(zip(a, t)):
             if int(tt) in tokset:
                 dX[pos[int(tt)]] += dx_rows[r]
@@ -410,8 +439,8 @@ def backward(X, W13, W2, idx, gate, dY, tokens=None, experts=None, mode="bf16"):
         if e in want_e:
             ei = exp_list.index(e)
             # contraction over the expert's tokens (column-wise blocks)
-            dW13[ei] = qb(X[t], 0).T @ qb(dh, 0)
-            dW2[ei] = qb(A_saved, 0).T @ qb(stb(g * dYt), 0)
+            dW13[ei] = qb(X[t], "bwd.X_dw").T @ qb(dh, "bwd.dh_dw")
+            dW2[ei] = qb(A_saved, "bwd.A_dw").T @ qb(stb(g * dYt), "bwd.gdY_dw")
     return dict(dX=dX, dgate=dgate, dW13=dW13, dW2=dW2)
 
 

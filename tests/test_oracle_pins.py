@@ -68,6 +68,25 @@ def test_route_neg_inf_experts_never_selected():
     assert np.isfinite(gate).all()
 
 
+def test_route_inputs_outside_the_softmax_domain():
+    """A token whose logits are all -inf is routed to experts 0..k-1 (equal
+    keys, ascending index, as a full sort gives) with zero gates; a NaN logit
+    routes like -inf; a token with fewer than k finite logits gives its -inf
+    slots gate 0 and its finite ones the softmax of the finite logits."""
+    lg = np.array([[-np.inf] * 6,
+                   [0.5, np.nan, 2.0, np.nan, -1.0, 0.0],
+                   [1.0, -np.inf, -np.inf, 3.0, -np.inf, -np.inf]], np.float32)
+    idx, gate = O.route(lg, 3)
+    assert list(idx[0]) == [0, 1, 2] and (gate[0] == 0).all()
+    nan_as_inf = np.where(np.isnan(lg[1]), -np.inf, lg[1])
+    i1, g1 = O.route(nan_as_inf[None], 3)
+    assert list(idx[1]) == list(i1[0]) == _bruteforce_topk(nan_as_inf, 3)
+    assert np.array_equal(gate[1], g1[0]) and np.isfinite(gate).all()
+    assert list(idx[2]) == [3, 0, 1]
+    assert gate[2, 2] == 0
+    assert np.allclose(gate[2, :2], scipy.special.softmax([3.0, 1.0]), rtol=1e-15, atol=0)
+
+
 def test_route_backward_finite_difference():
     """d(logits) through the renormalised top-k softmax vs central
     differences of sum(gate * w) with the selection held fixed."""
