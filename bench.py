@@ -59,6 +59,8 @@ def _args():
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--workload", default="235b", choices=[k for k in CONFIGS if k != "tiny"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-per-config", action="store_true",
+                   help="skip the shorter runs of the other workloads and modes")
     # smaller variants of the workload, for profiler captures
     p.add_argument("--tokens", type=int, default=None, help="override T")
     p.add_argument("--experts", type=int, default=None, help="override E")
@@ -271,6 +273,90 @@ def run_reference(args):
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }))
+
+
+def _per_config(cfg, mode, d, steps, warmup, peaks):
+    """fwd / bwd / step ms of one workload and mode on already-resident inputs
+    ``d`` (device tensors), with the grouped-GEMM launch times from the
+    library's event hook (in the MXFP8 modes that bracket also holds the
+    quantise passes between the GEMM launches)."""
+    import torch
+
+    import mixture_experts_layer_18_gb300 as M
+    from mixture_experts_layer_18_gb300.layer import MoELayer
+    L = MoELayer(cfg.T, cfg.H, cfg.E, cfg.I, cfg.k, mode=mode)
+    io = L.empty_io()
+    dl = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device="cuda")
+
+    def fwd():
+        L.route(d["logits"])
+        L.forward(d["X"], d["W13"], d["W2"], io["Y"])
+
+    def bwd():
+        L.backward(d["dY"], d["W13"], d["W2"], io["dX"], io["dW13"], io["dW2"], io["dgate"])
+        L.route_backward(io["dgate"], dl)
+
+    for _ in range(warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    pf = [(ev(), ev()) for _ in range(steps)]
+    pb = [(ev(), ev()) for _ in range(steps)]
+    for a, b in pf + pb:       # materialise the event handles (torch creates them lazily)
+        a.record()
+        b.record()
+    t0, t1 = ev(), ev()
+    torch.cuda.synchronize()
+    t0.record()
+    for i in range(steps):
+        M.moe_set_gemm_events(M.MOE_WS_FORWARD, pf[i][0].cuda_event, pf[i][1].cuda_event)
+        fwd()
+        M.moe_set_gemm_events(M.MOE_WS_BACKWARD, pb[i][0].cuda_event, pb[i][1].cuda_event)
+        bwd()
+    t1.record()
+    torch.cuda.synchronize()
+    if L.device_status() != 0:
+        raise RuntimeError(f"{cfg.name} {mode}: device status {L.device_status()}")
+    step = t0.elapsed_time(t1) / steps
+
+    def timed(fn):
+        a, b = ev(), ev()
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    fwd_ms, bwd_ms = timed(fwd), timed(bwd)
+    gf = statistics.mean(a.elapsed_time(b) for a, b in pf)
+    gb = statistics.mean(a.elapsed_time(b) for a, b in pb)
+    out = {"workload": _workload_desc(cfg), "mode": mode, "steps": steps, "warmup": warmup,
+           "ms_per_step": step, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+           "tflops": (cfg.fwd_flops() + cfg.bwd_flops()) / (step * 1e-3) / 1e12,
+           "fwd_tflops": cfg.fwd_flops() / (fwd_ms * 1e-3) / 1e12,
+           "bwd_tflops": cfg.bwd_flops() / (bwd_ms * 1e-3) / 1e12}
+    if mode != "f32":
+        peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+        pk_f = peak * (2 if mode == "mxfp8" else 1)
+        pk_b = peak * (2 if mode in ("mxfp8", "fp8_bwd") else 1)
+        out["gemm"] = {
+            "fwd_launch_ms": gf, "bwd_launch_ms": gb,
+            "fwd_frac": cfg.fwd_flops() / (gf * 1e-3) / 1e12 / pk_f,
+            "bwd_frac": cfg.bwd_flops() / (gb * 1e-3) / 1e12 / pk_b,
+            "peak_tflops_fwd": pk_f, "peak_tflops_bwd": pk_b,
+            "note": ("bf16 sustained measured peak" + (" x 2 (nominal fp8/bf16 ratio) where MXFP8"
+                     if mode != "bf16" else "")
+                     + ("; the bracket includes the quantise passes between the GEMM launches"
+                        if mode != "bf16" else ""))}
+    del L, io
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_gpu(args):
@@ -516,6 +602,27 @@ def run_gpu(args):
         "gpu_launches": LAUNCHES_PER_STEP[args.mode] * K,
         "clocks": clk,
     }
+    # ---- the other workloads of the metric (shorter runs; the headline value
+    # above stays the 235B bf16 step)
+    if world == 1 and not args.no_per_config and not (args.tokens or args.experts):
+        pc = []
+        if args.workload == "235b" and args.mode == "bf16":
+            for m in ("mxfp8", "fp8_bwd"):
+                pc.append(_per_config(CONFIGS["235b_mxfp8"], m, d, 10, 3, peaks))
+        del d
+        torch.cuda.empty_cache()
+        c30 = CONFIGS["30b"]
+        i30 = make_inputs(c30)
+        d30 = {k: dev(v) for k, v in i30.items()}
+        pc.append(_per_config(c30, "bf16", d30, 10, 3, peaks))
+        d30["logits"] = dev(make_inputs(CONFIGS["30b_zipf"], parts=("logits",))["logits"])
+        pc.append(_per_config(CONFIGS["30b_zipf"], "bf16", d30, 10, 3, peaks))
+        del d30
+        ct = CONFIGS["tiny"]
+        dt_ = {k: dev(v) for k, v in make_inputs(ct).items()}
+        pc.append(_per_config(ct, "f32", dt_, 10, 3, peaks))
+        out["per_config"] = pc
+
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         experts = list(range(CPU_SAMPLE_EXPERTS))
         dt, fl = _oracle_sample(cfg, inp, experts)

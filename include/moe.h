@@ -57,7 +57,9 @@ typedef enum {
   MOE_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement      */
   MOE_ERR_CUDA = 3,         /* a CUDA launch or driver call failed              */
   MOE_ERR_TIMEOUT = 4,      /* device: a bounded wait ran out (kernel returned) */
-  MOE_ERR_BAD_INDEX = 5     /* device: an expert index outside [0, E) was seen  */
+  MOE_ERR_BAD_INDEX = 5,    /* device: an expert index outside [0, E) was seen  */
+  MOE_ERR_BAD_INPUT = 6     /* device: an input the operation is not defined for
+                               (a NaN logit; a token whose logits are all -inf) */
 } moe_status;
 
 typedef enum {
@@ -143,8 +145,14 @@ moe_status moe_saved_layout_of(const moe_dims* dims, moe_saved_layout* out);
 
 /* Router and permutation builder ([MM] "In brief"; [TE] 02 and
  * "Optimisation 2": local reordering of token copies by expert).
- *   logits  float [T, E] (device).  Must not contain NaN; -inf experts are
- *           never chosen while top_k finite logits remain.
+ *   logits  float [T, E] (device).  -inf experts are never chosen while
+ *           top_k finite logits remain (a token with fewer finite logits
+ *           gets its -inf slots in ascending expert order, with gate 0).
+ *           A token whose logits are all -inf has no softmax: it is routed
+ *           to experts 0..top_k-1 with every gate 0 (it contributes nothing
+ *           to the layer's output) and *dev_status gets MOE_ERR_BAD_INPUT.
+ *           A NaN logit is read as -inf and also reported as
+ *           MOE_ERR_BAD_INPUT.
  *   out     all seven arrays of moe_route_out (device, caller-owned).
  *   ws      MOE_WS_ROUTE workspace.
  * Indices, counts and offsets are deterministic and independent of the GPU. */
@@ -161,9 +169,13 @@ moe_status moe_route(const moe_dims* dims, const float* logits,
  *   Scratch: a library-owned device array of 512 KiB (131072 int32) that
  *   every GPU which loads the library holds until process exit.  Requires
  *   2 * E * ceil(T / 128) <= 131072, else MOE_ERR_INVALID_ARG (no launch).
- *   The first call on a device looks up the array's device address with that
- *   device current (no allocation); make that first call before any stream
- *   capture.  The library calls no cudaMalloc / cudaFree here.
+ *   The first call in each CUDA context (each device's primary context,
+ *   and again after a device reset, which creates a new context holding a
+ *   new copy of the array) looks up the array's device address with that
+ *   device current (no allocation) and caches it; make that first call
+ *   before any stream capture (a call during capture that would need the
+ *   lookup returns MOE_ERR_CUDA and launches nothing).  The library calls
+ *   no cudaMalloc / cudaFree here; the cache is safe across host threads.
  *   All calls share the one array: calls whose work can overlap on the GPU
  *   (different streams, or different host threads) race and must be ordered
  *   by the caller.  Each call writes every scratch entry it reads. */
@@ -276,6 +288,14 @@ const char* moe_status_string(moe_status s);
  * Process-wide; not thread-safe against concurrent calls. */
 enum { MOE_DEBUG_NEVER_READY = 1, MOE_DEBUG_SINGLE_CTA = 2, MOE_DEBUG_SPLIT_BACKWARD = 4 };
 void moe_set_debug(int flags, int64_t wait_limit_ns);
+
+/* Diagnosis hook: a bounded side load.  Launches `ctas` thread blocks on
+ * `stream`, each holding `smem_bytes` of shared memory (at most 227 KB) for
+ * `duration_ns` (at most one second) and then returning, so that a test can
+ * run the layer while part of the GPU is busy (the co-scheduled backward
+ * must still finish: its launch starts only once all of its CTAs fit).
+ * MOE_ERR_INVALID_ARG outside those limits. */
+moe_status moe_debug_occupy(int ctas, int smem_bytes, int64_t duration_ns, void* stream);
 
 /* Timing hook for kernel-level measurement.  `start` and `stop` are
  * cudaEvent_t handles (as void*) created by the caller.  The next call of the

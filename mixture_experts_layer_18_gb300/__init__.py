@@ -15,17 +15,17 @@ from .builder import LIB, build  # noqa: F401
 
 __all__ = [
     "MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_CUDA",
-    "MOE_ERR_TIMEOUT", "MOE_ERR_BAD_INDEX", "MOE_F32", "MOE_BF16", "MOE_MXFP8",
+    "MOE_ERR_TIMEOUT", "MOE_ERR_BAD_INDEX", "MOE_ERR_BAD_INPUT", "MOE_F32", "MOE_BF16", "MOE_MXFP8",
     "MOE_FP8_BWD", "MOE_WS_ROUTE", "MOE_WS_FORWARD", "MOE_WS_BACKWARD",
     "MOE_DEBUG_NEVER_READY", "MOE_DEBUG_SINGLE_CTA", "MOE_DEBUG_SPLIT_BACKWARD", "moe_dims", "moe_route_out", "moe_saved_layout",
     "lib", "header_functions", "moe_max_rows", "moe_workspace_size",
     "moe_saved_layout_of", "moe_route", "moe_route_noalloc", "moe_route_backward", "moe_forward", "moe_backward",
-    "moe_quantize_mxfp8", "moe_quantize_mxfp8_dual", "moe_status_string", "moe_set_debug", "moe_set_gemm_events",
+    "moe_quantize_mxfp8", "moe_quantize_mxfp8_dual", "moe_status_string", "moe_set_debug", "moe_set_gemm_events", "moe_debug_occupy",
     "MoEError",
 ]
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3
-MOE_ERR_TIMEOUT, MOE_ERR_BAD_INDEX = 4, 5
+MOE_ERR_TIMEOUT, MOE_ERR_BAD_INDEX, MOE_ERR_BAD_INPUT = 4, 5, 6
 MOE_F32, MOE_BF16, MOE_MXFP8, MOE_FP8_BWD = 0, 1, 2, 3
 MOE_WS_ROUTE, MOE_WS_FORWARD, MOE_WS_BACKWARD = 0, 1, 2
 MOE_DEBUG_NEVER_READY = 1
@@ -80,6 +80,7 @@ _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [_c_int]),
     "moe_set_debug": (None, [_c_int, _i64]),
     "moe_set_gemm_events": (None, [_c_int, _vp, _vp]),
+    "moe_debug_occupy": (_c_int, [_c_int, _c_int, _i64, _vp]),
 }
 
 _lib = None
@@ -167,6 +168,10 @@ def moe_status_string(code: int) -> str:
 
 def moe_set_debug(flags: int, wait_limit_ns: int = 0) -> None:
     lib().moe_set_debug(flags, wait_limit_ns)
+
+
+def moe_debug_occupy(ctas: int, smem_bytes: int, duration_ns: int, stream) -> int:
+    return lib().moe_debug_occupy(ctas, smem_bytes, duration_ns, stream)
 
 
 def moe_set_gemm_events(which: int, start, stop) -> None:

@@ -214,12 +214,15 @@ __global__ void __launch_bounds__(256) transpose_f32_kernel(const float* __restr
 }
 
 int num_sms() {
-  static int sms[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-  return sms[dev] > 0 ? sms[dev] : 1;
+  static CtxCache<int> cache;
+  int n = 0;
+  cache.get(&n, [](int* v) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev);
+    return e;
+  });
+  return n > 0 ? n : 1;
 }
 
 int grid_for_rows(int64_t rows) {

@@ -1178,59 +1178,73 @@ bool make_tmap_out3(CUtensorMap* m, void* base, int64_t E, int64_t M, int64_t N)
 }
 
 int sm_count() {
-  static int sms[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-  return sms[dev] > 0 ? sms[dev] : 1;
+  static CtxCache<int> cache;
+  int n = 0;
+  cache.get(&n, [](int* v) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev);
+    return e;
+  });
+  return n > 0 ? n : 1;
 }
 
+// `gang`: tiles of this launch wait on tiles of other CTAs, so it is made a
+// cooperative launch: the GPU starts it only once every CTA of the grid can
+// be resident, instead of starting the CTAs that fit while other work (a
+// kernel on another stream) holds the rest of the SMs, whose tiles the
+// started ones would then wait for.
 template <typename In, typename Out, int BN, int PAIR>
-cudaError_t launch_typed(const EngineParams& P, int64_t tile_bound, cudaStream_t s) {
+cudaError_t launch_typed(const EngineParams& P, int64_t tile_bound, bool gang, cudaStream_t s) {
   using C = Cfg<In, BN, PAIR>;
   auto kern = moe_gemm_kernel<In, Out, BN, PAIR>;
-  static bool attr_set[64] = {false};
-  static int max_clusters[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (PAIR == 2) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = PAIR;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  // Per context: the shared-memory opt-in, and for pairs the number of
+  // clusters resident at once (tiles wait on other tiles, so the grid never
+  // exceeds it).
+  static CtxCache<int> resident;
+  int max_units = 0;
+  cudaError_t e = resident.get(&max_units, [&](int* v) {
+    cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
-  if constexpr (PAIR == 1) {
-    int grid = sm_count();
-    if (tile_bound < grid) grid = (int)(tile_bound < 1 ? 1 : tile_bound);
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(P);
-    return cudaGetLastError();
-  } else {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(C::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (!max_clusters[dev]) {
-      // every cluster must be resident at once (tiles wait on other tiles)
-      cfg.gridDim = dim3(2 * (sm_count() / 2), 1, 1);
+    if (r != cudaSuccess) return r;
+    if constexpr (PAIR == 1) {
+      *v = sm_count();
+      return cudaSuccess;
+    } else {
+      cudaLaunchConfig_t q = cfg;
+      q.gridDim = dim3(2 * (sm_count() / 2), 1, 1);
       int n = 0;
-      cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-      if (e != cudaSuccess || n < 1) return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
-      max_clusters[dev] = n;
+      r = cudaOccupancyMaxActiveClusters(&n, kern, &q);
+      if (r == cudaSuccess && n < 1) r = cudaErrorInvalidConfiguration;
+      *v = n;
+      return r;
     }
-    int64_t clusters = max_clusters[dev];
-    if (tile_bound < clusters) clusters = tile_bound < 1 ? 1 : tile_bound;
-    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
-    return cudaLaunchKernelEx(&cfg, kern, P);
+  });
+  if (e != cudaSuccess) return e;
+  int64_t units = max_units;
+  if (tile_bound < units) units = tile_bound < 1 ? 1 : tile_bound;
+  cfg.gridDim = dim3((unsigned)(PAIR * units), 1, 1);
+  if (gang) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    cfg.numAttrs = ++na;
   }
+  return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
 }  // namespace
@@ -1254,6 +1268,7 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
   const int pair = (es == 2 || es == 1) && L.BN >= 128 && !(debug_flags() & MOE_DEBUG_SINGLE_CTA)
                        ? 2 : 1;
   int64_t tile_bound = 0;
+  bool gang = false;
   const int64_t mblocks_max = (L.max_rows + 127) / 128;
   for (int p = 0; p < L.nprob; ++p) {
     const GemmDesc& d = L.prob[p];
@@ -1263,6 +1278,7 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
     g.b_mn = d.b_mn;
     g.dep = d.dep;
     g.signal = d.signal;
+    gang = gang || d.dep != DEP_NONE;
     g.M = d.M;
     g.N = d.N;
     g.K = d.K;
@@ -1323,23 +1339,23 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
   }
   if (es == 2 && pair == 2) {
     switch (L.BN) {
-      case 256: return launch_typed<__nv_bfloat16, __nv_bfloat16, 256, 2>(P, tile_bound, s);
-      case 128: return launch_typed<__nv_bfloat16, __nv_bfloat16, 128, 2>(P, tile_bound, s);
+      case 256: return launch_typed<__nv_bfloat16, __nv_bfloat16, 256, 2>(P, tile_bound, gang, s);
+      case 128: return launch_typed<__nv_bfloat16, __nv_bfloat16, 128, 2>(P, tile_bound, gang, s);
     }
   } else if (es == 2) {
     switch (L.BN) {
-      case 256: return launch_typed<__nv_bfloat16, __nv_bfloat16, 256, 1>(P, tile_bound, s);
-      case 128: return launch_typed<__nv_bfloat16, __nv_bfloat16, 128, 1>(P, tile_bound, s);
-      case 64: return launch_typed<__nv_bfloat16, __nv_bfloat16, 64, 1>(P, tile_bound, s);
+      case 256: return launch_typed<__nv_bfloat16, __nv_bfloat16, 256, 1>(P, tile_bound, gang, s);
+      case 128: return launch_typed<__nv_bfloat16, __nv_bfloat16, 128, 1>(P, tile_bound, gang, s);
+      case 64: return launch_typed<__nv_bfloat16, __nv_bfloat16, 64, 1>(P, tile_bound, gang, s);
     }
   } else if (es == 1) {   // MXFP8 operands, bf16 outputs
-    if (L.BN == 256 && pair == 2) return launch_typed<uint8_t, __nv_bfloat16, 256, 2>(P, tile_bound, s);
-    if (L.BN == 256) return launch_typed<uint8_t, __nv_bfloat16, 256, 1>(P, tile_bound, s);
+    if (L.BN == 256 && pair == 2) return launch_typed<uint8_t, __nv_bfloat16, 256, 2>(P, tile_bound, gang, s);
+    if (L.BN == 256) return launch_typed<uint8_t, __nv_bfloat16, 256, 1>(P, tile_bound, gang, s);
   } else if (es == 4) {
     switch (L.BN) {
-      case 256: return launch_typed<float, float, 256, 1>(P, tile_bound, s);
-      case 128: return launch_typed<float, float, 128, 1>(P, tile_bound, s);
-      case 64: return launch_typed<float, float, 64, 1>(P, tile_bound, s);
+      case 256: return launch_typed<float, float, 256, 1>(P, tile_bound, gang, s);
+      case 128: return launch_typed<float, float, 128, 1>(P, tile_bound, gang, s);
+      case 64: return launch_typed<float, float, 64, 1>(P, tile_bound, gang, s);
     }
   }
   *st = MOE_ERR_UNSUPPORTED;

@@ -2,9 +2,12 @@
 // kernel translation units (not part of the public interface).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
+
+#include <mutex>
 
 #include "moe.h"
 
@@ -122,5 +125,58 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
 // debug / limits (api.cu)
 uint64_t wait_limit_ns();
 int debug_flags();
+
+// Identity of the calling thread's current CUDA context (the current
+// device's primary context is bound first if none is), unique over the
+// process lifetime: a context created after a device reset gets a new one.
+cudaError_t current_context_id(unsigned long long* id);
+
+// Host values that belong to a CUDA context (kernel attributes, occupancy,
+// device addresses of module variables), cached per context and safe to use
+// from several host threads.  get() returns the current context's value,
+// computing it with make(&value) the first time the context is seen (only a
+// cudaSuccess result is stored); find() only looks.
+template <typename V, int N = 32>
+class CtxCache {
+ public:
+  template <typename F>
+  cudaError_t get(V* out, F&& make) {
+    unsigned long long id = 0;
+    cudaError_t e = current_context_id(&id);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (lookup(id, out)) return cudaSuccess;
+    V v{};
+    e = make(&v);
+    if (e != cudaSuccess) return e;
+    const int slot = n_ < N ? n_++ : (next_++ % N);   // the oldest entry goes when full
+    ids_[slot] = id;
+    vals_[slot] = v;
+    *out = v;
+    return cudaSuccess;
+  }
+  cudaError_t find(V* out, bool* found) {
+    unsigned long long id = 0;
+    cudaError_t e = current_context_id(&id);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu_);
+    *found = lookup(id, out);
+    return cudaSuccess;
+  }
+
+ private:
+  bool lookup(unsigned long long id, V* out) const {
+    for (int i = 0; i < n_; ++i)
+      if (ids_[i] == id) {
+        *out = vals_[i];
+        return true;
+      }
+    return false;
+  }
+  std::mutex mu_;
+  unsigned long long ids_[N] = {};
+  V vals_[N] = {};
+  int n_ = 0, next_ = 0;
+};
 
 }  // namespace moe

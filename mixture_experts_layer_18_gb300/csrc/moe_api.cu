@@ -2,6 +2,7 @@
 // carving, and the launch sequence of each call on the caller's stream.
 #include <atomic>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -37,7 +38,47 @@ struct EventScope {   // records the pending hook's events around a launch group
 uint64_t wait_limit_ns() { return (uint64_t)g_wait_ns.load(); }
 int debug_flags() { return g_debug_flags.load(); }
 
+cudaError_t current_context_id(unsigned long long* id) {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  if (!get_current || !get_id) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) {
+    // no context bound to this thread yet: bind the current device's
+    // primary context (cudaSetDevice initialises it)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return e;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorInitializationError;
+  }
+  return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorContextIsDestroyed;
+}
+
 namespace {
+
+// Holds its CTA (and the CTA's shared memory) for `ns` nanoseconds, then
+// returns: the bounded side load of moe_debug_occupy.
+__global__ void occupy_kernel(uint64_t ns) {
+  extern __shared__ uint8_t hold[];
+  if (threadIdx.x == 0) reinterpret_cast<volatile uint8_t*>(hold)[0] = 1;
+  const uint64_t t0 = global_ns();
+  while (global_ns() - t0 < ns) __nanosleep(2000);
+}
 
 constexpr int GK_FWD1 = 0, GK_FWD2 = 1, GK_BWD_D = 2, GK_BWD_DX = 3, GK_DW = 4;
 constexpr int DEP_NONE = 0, DEP_MBLOCK = 1, DEP_EXPERT = 2;
@@ -477,6 +518,7 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_TIMEOUT: return "device wait timed out";
     case MOE_ERR_BAD_INDEX: return "index out of range";
+    case MOE_ERR_BAD_INPUT: return "input outside the operation's domain";
   }
   return "unknown status";
 }
@@ -490,6 +532,23 @@ void moe_set_gemm_events(int which, void* start, void* stop) {
 void moe_set_debug(int flags, int64_t wait_limit_ns) {
   g_debug_flags.store(flags);
   g_wait_ns.store(wait_limit_ns > 0 ? wait_limit_ns : 1000000000LL);
+}
+
+moe_status moe_debug_occupy(int ctas, int smem_bytes, int64_t duration_ns, void* stream) {
+  if (ctas < 1 || ctas > 4096 || smem_bytes < 0 || smem_bytes > 227 * 1024 || duration_ns <= 0 ||
+      duration_ns > 1000000000LL)
+    return MOE_ERR_INVALID_ARG;
+  static CtxCache<int> attr;
+  int done = 0;
+  if (attr.get(&done, [](int* v) {
+        *v = 1;
+        return cudaFuncSetAttribute(occupy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    227 * 1024);
+      }) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  occupy_kernel<<<ctas, 32, smem_bytes, static_cast<cudaStream_t>(stream)>>>(
+      (uint64_t)duration_ns);
+  return cuda_status(cudaGetLastError());
 }
 
 moe_status moe_route(const moe_dims* d, const float* logits, const moe_route_out* out, void* ws,
@@ -823,8 +882,6 @@ moe_status moe_quantize_mxfp8(const void* src, int R, int C, int ld, int axis,
 // per-block expert histograms and their exclusive bases, 2 * E * ceil(T/128)
 // int32) lives in one file-scope device array instead of a caller workspace.
 // ---------------------------------------------------------------------------
-#include <mutex>
-
 namespace moe {
 namespace {
 
@@ -832,26 +889,26 @@ constexpr int64_t kNoAllocRouteInts = 131072;   // 512 KiB of int32 scratch
 __device__ __align__(256) int32_t g_route_scratch[kNoAllocRouteInts];
 
 // In host code g_route_scratch names a host-side stand-in, not the device
-// array, so its device address is looked up once per device (with that device
-// current) and cached.
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-int32_t* g_scratch_ptr[kMaxDevices] = {};
+// array, so its device address is looked up with the device current, once per
+// CUDA context (a context created after a device reset holds a new copy of
+// the array and gets a new lookup), and cached.  The lookup is not made while
+// the stream is being captured into a graph.
+CtxCache<int32_t*> g_scratch_addr;
 
-cudaError_t route_scratch_ptr(int32_t** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+cudaError_t route_scratch_ptr(cudaStream_t s, int32_t** out) {
+  bool found = false;
+  cudaError_t e = g_scratch_addr.find(out, &found);
+  if (e != cudaSuccess || found) return e;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(s, &cs);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (cs != cudaStreamCaptureStatusNone) return cudaErrorStreamCaptureUnsupported;
+  return g_scratch_addr.get(out, [](int32_t** v) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_route_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = static_cast<int32_t*>(p);
-  }
-  *out = g_scratch_ptr[dev];
-  return cudaSuccess;
+    const cudaError_t r = cudaGetSymbolAddress(&p, g_route_scratch);
+    if (r == cudaSuccess) *v = static_cast<int32_t*>(p);
+    return r;
+  });
 }
 
 }  // namespace
@@ -865,14 +922,14 @@ extern "C" moe_status moe_route_noalloc(const moe_dims* d, const float* logits,
   if (d->T > 0 && !aligned16(logits)) return MOE_ERR_INVALID_ARG;
   const int64_t nb = ((int64_t)d->T + kRouteTokPerBlock - 1) / kRouteTokPerBlock;
   if (2 * nb * d->E > kNoAllocRouteInts) return MOE_ERR_INVALID_ARG;   // scratch too small
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* scratch = nullptr;
-  if (route_scratch_ptr(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  if (route_scratch_ptr(s, &scratch) != cudaSuccess) return MOE_ERR_CUDA;
   // Every scratch entry read below is first written by the same call (the
   // router writes all E x nb histogram entries, the scan all bases), so no
   // clearing is needed.
   int32_t* hist = scratch;
   int32_t* base = scratch + nb * d->E;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   MOE_TRY(launch_route(logits, d->T, d->E, d->top_k, out->topk_idx, out->gate, hist, dev_status, s));
   MOE_TRY(launch_permute(out->topk_idx, d->T, d->E, d->top_k, max_rows(d), hist, base, out->counts,
                          out->offsets, out->padded_offsets, out->row_of_assign,

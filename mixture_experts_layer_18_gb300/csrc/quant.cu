@@ -358,31 +358,26 @@ cudaError_t launch_quantize_dual(const void* src, int R, int C, int ld, const in
   const int64_t tiles = (int64_t)((R + kDualRows - 1) / kDualRows) * (C / 128);
   if (tiles == 0) return cudaSuccess;
   const __nv_bfloat16* x = (const __nv_bfloat16*)src;
-  // per device (the attribute belongs to a context): shared-memory opt-in
-  // and the resident block count, so the grid is exactly one wave and every
-  // block strides over the same number of tiles
-  static bool attr_set[64][3] = {};
-  static int resident[64][3] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  bool* attr_done = attr_set[dev];
+  // per context (the attribute belongs to one): shared-memory opt-in and the
+  // resident block count, so the grid is exactly one wave and every block
+  // strides over the same number of tiles
+  static CtxCache<int> resident[3];
   int blocks = 0;
   auto setup = [&](auto kern, size_t bytes, int which) {
-    if (!attr_done[which]) {
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
-          cudaSuccess)
-        return false;
-      int per_sm = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, bytes) != cudaSuccess ||
-          per_sm < 1)
-        return false;
-      int sms = 0;
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      resident[dev][which] = per_sm * (sms > 0 ? sms : 1);
-      attr_done[which] = true;
-    }
-    blocks = (int)(tiles < resident[dev][which] ? tiles : resident[dev][which]);
+    int n = 0;
+    const cudaError_t e = resident[which].get(&n, [&](int* v) {
+      cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+      if (r != cudaSuccess) return r;
+      int per_sm = 0, dev = 0, sms = 0;
+      r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, bytes);
+      if (r == cudaSuccess && per_sm < 1) r = cudaErrorInvalidConfiguration;
+      if (r == cudaSuccess) r = cudaGetDevice(&dev);
+      if (r == cudaSuccess) r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      *v = per_sm * (sms > 0 ? sms : 1);
+      return r;
+    });
+    if (e != cudaSuccess) return false;
+    blocks = (int)(tiles < n ? tiles : n);
     return true;
   };
   if (!gather) {

@@ -33,12 +33,15 @@ template <int VPL> struct RouteShape {
 // (independent shuffle chains, so their latencies overlap).  Lane l holds
 // logits l, l+32, l+64, ... of each token in registers.  k rounds of a warp
 // arg-max pick the largest remaining logit, ties to the lower expert index
-// (a total order for NaN-free input).  Slot j of the result is the j-th
-// pick.  Also builds this block's expert histogram.
+// (a total order: a NaN logit is read as -inf and reported as
+// MOE_ERR_BAD_INPUT).  Slot j of the result is the j-th pick.  A token whose
+// logits are all -inf has no softmax: it gets zero gates (it contributes
+// nothing to the layer) and MOE_ERR_BAD_INPUT.  Also builds this block's
+// expert histogram.
 template <int VPL>
 __global__ void __launch_bounds__(RouteShape<VPL>::THREADS) route_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,
-    float* __restrict__ gate, int32_t* __restrict__ block_hist, int nb) {
+    float* __restrict__ gate, int32_t* __restrict__ block_hist, int nb, int32_t* status) {
   constexpr int NT = RouteShape<VPL>::NT, ILP = RouteShape<VPL>::ILP;
   __shared__ int hist[kMaxE];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
@@ -56,7 +59,12 @@ __global__ void __launch_bounds__(RouteShape<VPL>::THREADS) route_kernel(
 #pragma unroll
       for (int q = 0; q < VPL; ++q) {
         const int e = q * 32 + lane;
-        v[i][q] = (e < E && t < T) ? __ldg(logits + (size_t)t * E + e) : 0.f;
+        float x = (e < E && t < T) ? __ldg(logits + (size_t)t * E + e) : 0.f;
+        if (x != x) {
+          report(status, MOE_ERR_BAD_INPUT);
+          x = -INFINITY;
+        }
+        v[i][q] = x;
         if (e >= E) taken[i] |= 1u << q;
       }
     }
@@ -108,13 +116,15 @@ __global__ void __launch_bounds__(RouteShape<VPL>::THREADS) route_kernel(
     for (int i = 0; i < ILP; ++i) {
       const int t = t0 + i;
       const float m = __shfl_sync(0xffffffffu, sel_v[i], 0);
-      const float w = lane < k ? expf(sel_v[i] - m) : 0.f;
+      const bool none = !(m > -INFINITY);   // every logit of the token is -inf
+      const float w = lane < k && !none ? expf(sel_v[i] - m) : 0.f;
       float sum = w;
 #pragma unroll
       for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      if (none && t < T && lane == 0) report(status, MOE_ERR_BAD_INPUT);
       if (t < T && lane < k) {
         topk_idx[(size_t)t * k + lane] = sel_e[i];
-        gate[(size_t)t * k + lane] = w / sum;
+        gate[(size_t)t * k + lane] = none ? 0.f : w / sum;
         atomicAdd(&hist[sel_e[i]], 1);
       }
     }
@@ -316,21 +326,20 @@ cudaError_t launch_route_backward(const int32_t* topk_idx, const float* gate, co
 }
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* topk_idx,
-                         float* gate, int32_t* block_hist, int32_t* /*status*/,
-                         cudaStream_t s) {
+                         float* gate, int32_t* block_hist, int32_t* status, cudaStream_t s) {
   const int nb = (T + kRouteTokPerBlock - 1) / kRouteTokPerBlock;
   if (nb == 0) return cudaSuccess;
   const int vpl = (E + 31) / 32;
   if (vpl <= 1)
-    route_kernel<1><<<nb, RouteShape<1>::THREADS, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
+    route_kernel<1><<<nb, RouteShape<1>::THREADS, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb, status);
   else if (vpl <= 4)
-    route_kernel<4><<<nb, RouteShape<4>::THREADS, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
+    route_kernel<4><<<nb, RouteShape<4>::THREADS, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb, status);
   else if (vpl <= 8)
-    route_kernel<8><<<nb, RouteShape<8>::THREADS, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
+    route_kernel<8><<<nb, RouteShape<8>::THREADS, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb, status);
   else if (vpl <= 16)
-    route_kernel<16><<<nb, RouteShape<16>::THREADS, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
+    route_kernel<16><<<nb, RouteShape<16>::THREADS, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb, status);
   else
-    route_kernel<32><<<nb, RouteShape<32>::THREADS, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb);
+    route_kernel<32><<<nb, RouteShape<32>::THREADS, 0, s>>>(logits, T, E, k, topk_idx, gate, block_hist, nb, status);
   return cudaGetLastError();
 }
 

@@ -103,3 +103,51 @@ def test_invalid_arguments_rejected_before_launch():
     assert rc == M.MOE_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert L.device_status() == 0
+
+
+def test_backward_while_half_the_gpu_is_busy():
+    """A bounded side kernel on another stream holds about half of the SMs
+    (one block with 200 KB of shared memory per SM, 76 blocks, 300 ms) while
+    a whole step runs with a 20 ms device wait limit.  The co-scheduled
+    backward's tiles wait on tiles of other CTAs, so its launch must not
+    start on the SMs that happen to be free and then wait for CTAs that
+    cannot be placed: the step finishes with status 0 and oracle parity."""
+    import torch
+    from mixture_experts_layer_18_gb300.layer import MoELayer
+    cfg = MoEConfig("busy", 4096, 1024, 16, 4, 512, "bf16")
+    inp = make_inputs(cfg, 1)
+    L = MoELayer(cfg.T, cfg.H, cfg.E, cfg.I, cfg.k, mode="bf16")
+    io = L.empty_io()
+    dev = {k: to_device(v) for k, v in inp.items()}
+    _step(L, io, dev)
+    torch.cuda.synchronize()
+    assert L.device_status() == 0
+    side = torch.cuda.Stream()
+    try:
+        M.moe_set_debug(0, 20_000_000)
+        L.clear_status()
+        torch.cuda.synchronize()
+        assert M.moe_debug_occupy(76, 200 * 1024, 300_000_000, side.cuda_stream) == M.MOE_OK
+        _step(L, io, dev)
+        torch.cuda.synchronize()
+    finally:
+        M.moe_set_debug(0, 0)
+    assert L.device_status() == 0
+    oi = {k: (F32View(v) if k != "logits" else v) for k, v in inp.items()}
+    idx, gate = O.route(inp["logits"], cfg.k)
+    tokens = np.arange(0, cfg.T, 97)
+    Y = O.forward(oi["X"], oi["W13"], oi["W2"], idx, gate, tokens=tokens)
+    g = O.backward(oi["X"], oi["W13"], oi["W2"], idx, gate, oi["dY"], tokens=tokens,
+                   experts=[0, 9])
+    assert rel_err(to_f64(io["Y"][tokens]), Y) <= TOL_BF16
+    assert rel_err(to_f64(io["dX"][tokens]), g["dX"]) <= TOL_BF16
+    assert rel_err(to_f64(io["dgate"][tokens]), g["dgate"]) <= TOL_BF16
+    for i, e in enumerate([0, 9]):
+        assert rel_err(to_f64(io["dW13"][e]), g["dW13"][i]) <= TOL_BF16
+        assert rel_err(to_f64(io["dW2"][e]), g["dW2"][i]) <= TOL_BF16
+
+
+def test_occupy_hook_rejects_unbounded_requests():
+    assert M.moe_debug_occupy(0, 0, 1000, None) == M.MOE_ERR_INVALID_ARG
+    assert M.moe_debug_occupy(4, 300 * 1024, 1000, None) == M.MOE_ERR_INVALID_ARG
+    assert M.moe_debug_occupy(4, 1024, 2_000_000_000, None) == M.MOE_ERR_INVALID_ARG

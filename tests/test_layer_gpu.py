@@ -37,8 +37,10 @@ def _oracle_inputs(inp):
     return {k: (F32View(v) if k != "logits" else v) for k, v in inp.items()}
 
 
-def _check_small(cfg, seed=0, mode=None, tol=TOL_BF16):
+def _check_small(cfg, seed=0, mode=None, tol=TOL_BF16, x_scale=None):
     inp = make_inputs(cfg, seed)
+    if x_scale is not None:
+        inp["X"] = _scaled_bf16(inp["X"], x_scale)
     L, io = _run(cfg, inp, mode)
     oi = _oracle_inputs(inp)
     idx, gate = O.route(inp["logits"], cfg.k)
@@ -69,6 +71,13 @@ def _check_small(cfg, seed=0, mode=None, tol=TOL_BF16):
     return errs
 
 
+def _scaled_bf16(bits, f):
+    """bf16 bit array times a power of two f (exact)."""
+    from workloads import bf16_bits_to_f32
+    v = (bf16_bits_to_f32(bits) * np.float32(f)).astype(np.float32)
+    return (v.view(np.uint32) >> 16).astype(np.uint16)
+
+
 def test_tiny_fp32_full():
     _check_small(CONFIGS["tiny"])
 
@@ -97,6 +106,14 @@ def test_small_shapes_single_cta_tiles(name):
         _check_small(SMALL[name])
     finally:
         M.moe_set_debug(0, 0)
+
+
+@pytest.mark.parametrize("name", ["bf16_a", "bf16_b"])
+def test_large_preactivations(name):
+    """Inputs scaled by 32: pre-activations reach |u| ~ 150, so exp(-u)
+    overflows to inf in the SiLU and sigmoid of the epilogues (their limits,
+    0 and u, must come out) and the activations reach ~10^4."""
+    _check_small(SMALL[name], seed=2, x_scale=32.0)
 
 
 def test_skewed_routing_with_empty_experts():

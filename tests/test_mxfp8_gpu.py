@@ -38,8 +38,12 @@ SMALL = [MoEConfig("mx_a", 512, 256, 8, 2, 256, "bf16"),
 
 @pytest.mark.parametrize("mode", ["mxfp8", "fp8_bwd"])
 @pytest.mark.parametrize("cfg", SMALL, ids=[c.name for c in SMALL])
-def test_small_shapes_full(cfg, mode):
+def test_small_shapes_full(cfg, mode, x_scale=None):
     inp = make_inputs(cfg)
+    if x_scale is not None:
+        from workloads import bf16_bits_to_f32
+        v = (bf16_bits_to_f32(inp["X"]) * np.float32(x_scale)).astype(np.float32)
+        inp["X"] = (v.view(np.uint32) >> 16).astype(np.uint16)
     L, io = _run(cfg, inp, mode)
     oi = _oracle_inputs(inp)
     idx, gate = O.route(inp["logits"], cfg.k)
@@ -60,6 +64,13 @@ def test_small_shapes_full(cfg, mode):
     # notice a silent bf16 fallback otherwise)
     gb = O.backward(oi["X"], oi["W13"], oi["W2"], idx, gate, oi["dY"], mode="bf16")
     assert rel_err(g["dW13"], gb["dW13"]) > 1e-3
+
+
+@pytest.mark.parametrize("mode", ["mxfp8", "fp8_bwd"])
+def test_large_preactivations(mode):
+    """Inputs scaled by 32 (|u| ~ 150: exp(-u) overflows in the epilogues'
+    SiLU and sigmoid; activations ~10^4, still far inside E4M3 x E8M0)."""
+    test_small_shapes_full(SMALL[0], mode, x_scale=32.0)
 
 
 @pytest.mark.parametrize("mode", ["mxfp8", "fp8_bwd"])
@@ -165,50 +176,63 @@ def test_activation_encodings_from_the_epilogue():
     assert rel_err(O.dequantize_mxfp8(q, sf, 0), A) <= 0.13
 
 
-@pytest.mark.parametrize("mode", ["mxfp8", "fp8_bwd"])
-def test_full_size_235b_sampled(mode):
-    """235B layer shape.  The oracle is run on k=1 sub-batches: Y, dX and
-    d(gate) of a few tokens are rebuilt from one-row sub-problems of each of
-    their assignments (every quantised operand of those rows is row-wise or a
-    weight, so the sub-problem quantises exactly as the full layer does), and
-    dW of a few experts from sub-batches holding all of an expert's
-    assignments in ascending order (the token-axis blocks of the full layer)."""
-    from workloads import bf16_bits_to_f32
-    cfg = CONFIGS["235b_mxfp8"]
+def _dw_experts(counts, rng):
+    """The largest expert, the smallest non-empty one, one whose count is not
+    a multiple of 32 (a partial token block) and a random non-empty one."""
+    nz = np.nonzero(counts)[0]
+    ex = [int(np.argmax(counts)), int(nz[np.argmin(counts[nz])])]
+    odd = [int(e) for e in nz if counts[e] % 32 and int(e) not in ex]
+    ex.append(odd[0])
+    rest = [int(e) for e in nz if int(e) not in ex]
+    ex.append(int(rng.choice(rest)))
+    return ex
+
+
+def _check_full_size(cfg, mode, n_tokens=64):
+    """Full-size layer in an MXFP8 mode, in the launch configuration the
+    benchmark times, against the oracle on sampled rows: Y, dX and d(gate)
+    of ``n_tokens`` tokens (every slot of each) and dW13 / dW2 of four
+    experts, element by element.  The oracle runs as per-expert sub-batches
+    in a spawned process pool (``_oracle_jobs``)."""
+    import _oracle_jobs
     inp = make_inputs(cfg)
     L, io = _run(cfg, inp, mode)
     idx, gate = O.route(inp["logits"], cfg.k)
     counts = np.bincount(idx.reshape(-1), minlength=cfg.E)
-
-    def f32(a):
-        return bf16_bits_to_f32(a) if a.dtype == np.uint16 else a
-
-    def sub(e, t, j):
-        one = np.zeros((len(t), 1), np.int32)
-        g = gate[t, j][:, None]
-        args = (f32(inp["X"][t]), f32(inp["W13"][e:e + 1]), f32(inp["W2"][e:e + 1]), one, g)
-        return O.forward(*args, mode=mode), O.backward(*args, f32(inp["dY"][t]), mode=mode)
-
+    assert np.array_equal(L.counts.cpu().numpy(), counts)
     rng = np.random.default_rng(2)
-    tokens = rng.choice(cfg.T, 1, replace=False)
-    Y = np.zeros((len(tokens), cfg.H))
-    dX = np.zeros((len(tokens), cfg.H))
-    dg = np.zeros((len(tokens), cfg.k))
-    for i, t in enumerate(tokens):
-        for j in range(cfg.k):
-            y, gb = sub(int(idx[t, j]), np.array([t]), np.array([j]))
-            Y[i] += y[0]
-            dX[i] += gb["dX"][0]
-            dg[i, j] = gb["dgate"][0, 0]
+    tokens = np.sort(rng.choice(cfg.T, n_tokens, replace=False))
+    dw_experts = _dw_experts(counts, rng)
+    Y, dX, dg, dws = _oracle_jobs.run_sampled(inp, idx, gate, tokens, dw_experts, mode)
     tol_f = TOL_MXFP8 if mode == "mxfp8" else TOL_BF16
     errs = {"Y": rel_err(to_f64(io["Y"][tokens]), Y),
             "dX": rel_err(to_f64(io["dX"][tokens]), dX),
             "dgate": rel_err(to_f64(io["dgate"][tokens]), dg)}
-    for e in sorted({int(np.argmax(counts)), int(np.argmin(counts))}):
-        t, j = np.nonzero(idx == e)
-        _, gb = sub(e, t, j)
-        errs[f"dW13[{e}]"] = rel_err(to_f64(io["dW13"][e]), gb["dW13"][0])
-        errs[f"dW2[{e}]"] = rel_err(to_f64(io["dW2"][e]), gb["dW2"][0])
+    for e in dw_experts:
+        errs[f"dW13[{e}]"] = rel_err(to_f64(io["dW13"][e]), dws[e][0])
+        errs[f"dW2[{e}]"] = rel_err(to_f64(io["dW2"][e]), dws[e][1])
     assert errs["Y"] <= tol_f, errs
     for k, v in errs.items():
         assert v <= TOL_MXFP8, (k, v, errs)
+    for e in np.nonzero(counts == 0)[0]:
+        assert (to_f64(io["dW13"][int(e)]) == 0).all() and (to_f64(io["dW2"][int(e)]) == 0).all()
+    return errs
+
+
+@pytest.mark.parametrize("mode", ["mxfp8", "fp8_bwd"])
+def test_full_size_235b_sampled(mode):
+    """235B layer shape: 64 tokens and four experts (largest, smallest, one
+    with a partial 32-row token block, one at random)."""
+    _check_full_size(CONFIGS["235b_mxfp8"], mode)
+
+
+def test_full_size_30b_zipf_mxfp8():
+    """30B shape with Zipf-skewed routing in mxfp8 mode: experts holding
+    nearly every token and eight empty ones go through the block-scaled
+    engine and the group-aware quantisers."""
+    import dataclasses
+    cfg = dataclasses.replace(CONFIGS["30b_zipf"], modes=("mxfp8",))
+    counts = np.bincount(O.route(make_inputs(cfg, parts=("logits",))["logits"], cfg.k)[0].reshape(-1),
+                         minlength=cfg.E)
+    assert (counts == 0).sum() >= 8 and counts.max() > 16000
+    _check_full_size(cfg, "mxfp8")

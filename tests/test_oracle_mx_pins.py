@@ -323,3 +323,33 @@ def test_flipped_axis_is_caught(name, monkeypatch):
     assert _all_pins_hold(L)
     monkeypatch.setitem(O.MX_AXES, name, 1 - O.MX_AXES[name])
     assert not _all_pins_hold(L), name
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_sampled_subbatches_equal_full_layer(mode):
+    """The per-expert sub-batches the full-size GPU tests give the oracle
+    (only the sampled tokens' assignments, or all of an expert's for its
+    weight gradients) reproduce the full layer's rows and weight gradients:
+    every operand of Y, dX and d(gate) is blocked along a row, and the token
+    blocks of the weight gradients see the whole expert."""
+    import _oracle_jobs
+    from workloads import MoEConfig, make_inputs
+    cfg = MoEConfig("sub", 300, 64, 6, 3, 64, "bf16")
+    inp = make_inputs(cfg, 3)
+    idx, gate = O.route(inp["logits"], cfg.k)
+    tokens = np.array([3, 77, 150, 299])
+    full_in = {k: _f(v) for k, v in inp.items()}
+    Yf = O.forward(full_in["X"], full_in["W13"], full_in["W2"], idx, gate, mode=mode)
+    gf = O.backward(full_in["X"], full_in["W13"], full_in["W2"], idx, gate, full_in["dY"], mode=mode)
+    Y, dX, dg, dws = _oracle_jobs.run_sampled(inp, idx, gate, tokens, [1, 4], mode, workers=2)
+    assert np.allclose(Y, Yf[tokens], rtol=1e-12, atol=1e-12)
+    assert np.allclose(dX, gf["dX"][tokens], rtol=1e-12, atol=1e-12)
+    assert np.allclose(dg, gf["dgate"][tokens], rtol=1e-12, atol=1e-12)
+    for e in (1, 4):
+        assert np.allclose(dws[e][0], gf["dW13"][e], rtol=1e-12, atol=1e-12)
+        assert np.allclose(dws[e][1], gf["dW2"][e], rtol=1e-12, atol=1e-12)
+
+
+def _f(a):
+    from workloads import bf16_bits_to_f32
+    return bf16_bits_to_f32(a).astype(np.float64) if a.dtype == np.uint16 else a

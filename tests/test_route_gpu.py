@@ -11,7 +11,7 @@ from _common import TOL_GATE, to_device
 pytestmark = pytest.mark.gpu
 
 
-def _run_route(logits_np, E, k, H=64, I=64):
+def _run_route(logits_np, E, k, H=64, I=64, status=0):
     import torch
     from mixture_experts_layer_18_gb300.layer import MoELayer
     T = logits_np.shape[0]
@@ -20,7 +20,7 @@ def _run_route(logits_np, E, k, H=64, I=64):
     lg = to_device(logits_np) if T else torch.empty((0, E), device="cuda")
     L.route(lg)
     torch.cuda.synchronize()
-    assert L.device_status() == 0
+    assert L.device_status() == status
     return L
 
 
@@ -85,3 +85,23 @@ def test_route_is_deterministic():
     b = _run_route(lg, cfg.E, cfg.k)
     for name in ("topk_idx", "gate", "row_of_assign", "assign_of_row", "padded_offsets"):
         assert np.array_equal(getattr(a, name).cpu().numpy(), getattr(b, name).cpu().numpy())
+
+
+def test_route_inputs_outside_the_softmax_domain():
+    """Tokens whose logits are all -inf (zero gates), NaN logits (read as
+    -inf) and tokens with fewer than k finite logits: indices and gates as
+    the oracle gives them, MOE_ERR_BAD_INPUT in the status word, and the
+    permutation still bit-exact."""
+    import mixture_experts_layer_18_gb300 as M
+    rng = np.random.default_rng(6)
+    lg = rng.standard_normal((300, 40)).astype(np.float32)
+    lg[3] = -np.inf
+    lg[150] = -np.inf
+    lg[7, [1, 5, 30]] = np.nan
+    lg[200, :] = -np.inf
+    lg[200, [9, 2]] = [0.5, 0.5]
+    L = _run_route(lg, 40, 4, status=M.MOE_ERR_BAD_INPUT)
+    _check(L, lg, 40, 4)
+    gate = L.gate.cpu().numpy()
+    assert (gate[[3, 150]] == 0).all() and np.isfinite(gate).all()
+    assert list(L.topk_idx.cpu().numpy()[3]) == [0, 1, 2, 3]
