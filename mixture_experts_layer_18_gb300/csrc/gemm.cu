@@ -26,6 +26,7 @@
 //          A: act [rows, I] K-major;  B: W2 as [E*I, H] N-major.
 //   BWD_D  D = dY_perm_e W2_e^T, epilogue dSwiGLU -> dh13, d(gate) partials
 //          A: dY_perm [rows, H] K-major;  B: W2 as [E*I, H] K-major.
+//          Block-scaled runs write dh13's MXFP8 encodings instead of bf16.
 //   BWD_DX dXp = dh13_e W13_e^T
 //          A: dh13 [rows, 2I] K-major;  B: W13 as [E*H, 2I] K-major.
 //   DW     dW_e = S_e^T G_e over the expert's rows (K = padded rows of e)
@@ -897,7 +898,17 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
           v[i] = a >= 0 ? dA * vv * sg * (1.f + u * (1.f - sg)) : 0.f;   // du
           w[i] = a >= 0 ? dA * si : 0.f;                                  // dv
         }
-        if constexpr (TS) {
+        if (C::MX && g.enc_row_q) {
+          // block-scaled runs: dh13 leaves as its two MXFP8 encodings (the
+          // dX and dW13 operands), decided from the bf16 values a stored
+          // dh13 would hold
+          stage_begin();   // the staging becomes the column-maximum scratch
+          encode_mx_block(v, row, ti.n0 + c, 2 * g.I, g.enc_row_q, g.enc_row_sf, g.enc_col_q,
+                          g.enc_col_sf, g.enc_col_kg, reinterpret_cast<float*>(sb0), lane);
+          encode_mx_block(w, row, g.I + ti.n0 + c, 2 * g.I, g.enc_row_q, g.enc_row_sf,
+                          g.enc_col_q, g.enc_col_sf, g.enc_col_kg, reinterpret_cast<float*>(sb0),
+                          lane);
+        } else if constexpr (TS) {
           stage_begin();
           stage_bf16_row(sb0, lane, v);
           stage_bf16_row(sb1, lane, w);
@@ -1320,9 +1331,10 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
                      : make_tmap(&g.tmB, d.b, es, d.b_rows, d.b_cols, BK,
                                  d.kind == GK_FWD1 ? L.BN / 2 : L.BN / pair));
     if (es != 4) {   // bf16 results: bulk-store views of the outputs
-      // every bf16 result leaves through a view built here; the one result
-      // that may be absent is FWD1's A when the epilogue encodes it instead
-      if (!d.out && !(d.kind == GK_FWD1 && d.enc_row_q)) {
+      // every bf16 result leaves through a view built here; the results
+      // that may be absent are FWD1's A and BWD_D's dh13 when the epilogue
+      // encodes them instead
+      if (!d.out && !((d.kind == GK_FWD1 || d.kind == GK_BWD_D) && d.enc_row_q)) {
         *st = MOE_ERR_INVALID_ARG;
         return cudaSuccess;
       }

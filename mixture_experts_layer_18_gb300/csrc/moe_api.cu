@@ -192,7 +192,8 @@ BwdWs bwd_ws(const moe_dims* d) {
   // gathers dY straight into its encodings
   w.dy_perm = o; o += mx_bwd(d) ? 0 : align256(rows * d->H * es);
   w.dyg_perm = o; o += mx_bwd(d) || gate_on_act(d) ? 0 : align256(rows * d->H * es);
-  w.dh13 = o; o += align256(rows * 2 * d->I * es);
+  // dh13 in bf16 (the MXFP8 backward keeps only its encodings, dh13r / dh13c)
+  w.dh13 = o; o += mx_bwd(d) ? 0 : align256(rows * 2 * d->I * es);
   w.dxp = o; o += align256(rows * d->H * es);
   w.partial = o; o += align256(rows * w.nt_d * sizeof(float));
   w.ready = o; o += align256(((rows + 127) / 128 + 1) * sizeof(int32_t));
@@ -394,14 +395,14 @@ moe_status forward_mx(const moe_dims* d, const void* X, const void* W13, const v
   return MOE_OK;
 }
 
-// Backward with MXFP8 GEMMs (modes mxfp8 and fp8_bwd).  dh13 must be
-// quantised before dX and dW13 can read it, so the gradient GEMMs run as
-// two launches: {D + dSwiGLU, dW2}, then {dX, dW13}.
+// Backward with MXFP8 GEMMs (modes mxfp8 and fp8_bwd).  The dSwiGLU epilogue
+// writes dh13's two encodings, which dX and dW13 read, so the gradient GEMMs
+// run as two launches: {D + dSwiGLU, dW2}, then {dX, dW13}.
 // The dY gather is fused into its quantisation: dY_perm and gate * dY_perm
 // exist only as their MXFP8 encodings.
 moe_status backward_mx(const moe_dims* d, const void* dY, const void* W13, const void* W2,
                        const moe_route_out* r, const void* x_perm, const void* h13,
-                       const void* act, void* dh13, void* dxp,
+                       const void* act, void* dxp,
                        float* partial, void* dW13, void* dW2, char* wsb, const BwdWs& w,
                        const MxSaved& sv, int32_t* dev_status, cudaStream_t s) {
   const int64_t rows = max_rows(d), rp = rows_pad(d);
@@ -442,7 +443,11 @@ moe_status backward_mx(const moe_dims* d, const void* dY, const void* W13, const
     gd.b = w2r.q; gd.b_rows = (int64_t)E * I; gd.b_cols = H; gd.b_expert_rows = I;
     gd.sfb = w2r.sf; gd.sfb_bytes = w2r.sf_bytes; gd.sfb_kg = H / 128;
     gd.N = I; gd.K = H; gd.I = I;
-    gd.out = dh13; gd.ld_out = 2 * I;
+    // dh13 leaves the dSwiGLU epilogue as its two MXFP8 encodings (row-wise
+    // for dX, column-wise along tokens for dW13), never as bf16
+    gd.enc_row_q = (uint8_t*)dh13r.q; gd.enc_row_sf = (uint8_t*)dh13r.sf;
+    gd.enc_col_q = (uint8_t*)dh13c.q; gd.enc_col_sf = (uint8_t*)dh13c.sf;
+    gd.enc_col_kg = rp / 128;
     gd.aux = h13; gd.ld_aux = 2 * I;
     gd.gate = r->gate; gd.assign_of_row = r->assign_of_row; gd.n_assign = d->T * d->top_k;
     gd.partial = partial;
@@ -457,7 +462,6 @@ moe_status backward_mx(const moe_dims* d, const void* dY, const void* W13, const
     MOE_TRY(launch_engine(L, s, &st));
     if (st != MOE_OK) return st;
   }
-  MOE_TRY(quant_both(dh13, rows, 2 * I, po + E, dh13r, &dh13c, s));
   if (!saved_mx) {
     MOE_TRY(quant_rows(W13, (int64_t)E * H, 2 * I, w13r, dev_status, s));
     MOE_TRY(quant_cols(x_perm, rows, H, po, E, xpc, dev_status, s));
@@ -714,7 +718,7 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
 
   if (mx_bwd(d)) {
     EventScope timing(MOE_WS_BACKWARD, s);
-    const moe_status st = backward_mx(d, dY, W13, W2, r, x_perm, h13, act, dh13, dxp,
+    const moe_status st = backward_mx(d, dY, W13, W2, r, x_perm, h13, act, dxp,
                                       partial, dW13, dW2, wb, w,
                                       mx_saved(d, sl, const_cast<char*>(sv)), dev_status, s);
     if (st != MOE_OK) return st;
