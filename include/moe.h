@@ -68,6 +68,9 @@ typedef enum {
   MOE_MXFP8 = 2,    /* bf16 storage, MXFP8 GEMMs in forward and backward          */
   MOE_FP8_BWD = 3   /* bf16 storage, bf16 forward GEMMs, MXFP8 backward GEMMs     */
 } moe_mode;
+/* The MXFP8 GEMMs (MOE_MXFP8 forward and backward, MOE_FP8_BWD backward)
+ * need I a multiple of 384 and H of 128; other shapes return
+ * MOE_ERR_UNSUPPORTED from the call that would run them. */
 
 /* Problem shape.  T tokens of width H, E experts of intermediate size I, each
  * token routed to top_k experts ([MM] "In brief": top-8 of 128).  Limits:
@@ -122,7 +125,13 @@ typedef struct {
  *   x_col   X_perm, 32-row blocks per expert group       (dW13 operand)
  *   act_col A, 32-row blocks per expert group             (dW2 operand)
  *   w13_row W13 [E*H, 2I], 32-column blocks along 2I      (dX operand)
- *   w2_row  W2 [E*I, H], 32-column blocks along H          (D operand)    */
+ *   w2_row  W2 [E*I, H], 32-column blocks along H          (D operand)
+ * The block-scaled GEMMs run tiles 192 columns wide, so the scales of the
+ * two weight operands (the GEMMs' B) sit in tile slots: row r of a weight
+ * with S rows per expert (S = H for w13_row, I for w2_row) has the scale
+ * MN index (r / S) * ceil(S / 192) * 256 + ((r % S) / 192) * 256 +
+ * (r % S) % 192 in the atom layout of moe_quantize_mxfp8_dual (each tile
+ * owns two whole atoms); the row-wise activations' scales use MN = row.   */
 typedef struct {
   size_t x_perm, h13, act;
   size_t x_col_q, x_col_sf, act_col_q, act_col_sf;

@@ -87,11 +87,13 @@ struct GemmProblem {
   uint8_t* enc_col_q;
   uint8_t* enc_col_sf;
   int64_t enc_col_kg;  // 128-row groups of the column-wise scale atoms
+  int64_t enc_col_ld;  // > 0: column-wise codes stored transposed with this pitch
   // MXFP8 operands: E8M0 scale atoms (512 B per 128 MN indices x 128 K),
   // read through [atoms * 4, 128]-byte views: atom i is rows 4i .. 4i + 3.
   CUtensorMap tmSFA;
   CUtensorMap tmSFB;
   int sfa_kg, sfb_kg;  // K groups of 128 in each operand's 2-D view
+  int64_t sfb_seg;     // B scales: MN slots per expert segment (0: one segment)
 };
 
 struct EngineParams {
@@ -99,6 +101,7 @@ struct EngineParams {
   int nprob;
   int E;
   const int32_t* padded_offsets;
+  const int32_t* counts;  // rows per expert (optional: weight-gradient K loops stop there)
   int32_t* ready;         // per-m-block counters, then one total at ready_all_index
   int ready_target;       // publications per m-block (n-tiles of the signalling problem)
   int ready_all_index;
@@ -118,43 +121,51 @@ struct Cfg {
   static constexpr int A_BYTES = 128 * 128;       // 128 rows x 128 bytes
   static constexpr int B_BYTES = BNL * 128;
   static constexpr int ATOM_BYTES = BK * 128;     // one MN-major column block
+  // Block-scaled tiles are 192 columns wide (kMxTileN): two accumulators of
+  // 192 columns and a scale slot per pipeline stage fit the 512 TMEM
+  // columns.  Their B operands come K-major (BNL = 96 rows per CTA of a
+  // pair), and the scales of a tile are two whole atoms (mx_tile_pos).
+  static_assert(!MX || BN == kMxTileN, "block-scaled tiles are 192 wide");
   // scale atoms per stage: A's 128 rows, and B's scales for all BN columns
   // of the MMA (each CTA of a pair needs every column's scale in its TMEM)
   static constexpr int SFA_BYTES = MX ? 512 : 0;
-  static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;
+  static constexpr int SFB_BYTES = MX ? 2 * 512 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;        // multiple of 1024
   static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;       // per stage, own region
   static constexpr int TX_BYTES = (STAGE_BYTES + SF_BYTES) * PAIR;   // bytes per full barrier
-  // Epilogue warps: 4 (one per TMEM lane quarter), or 8 for block-scaled
-  // pairs, whose single accumulator keeps the MMAs idle while it drains
-  // (two warps per quarter, each taking half of the tile's columns).
-  static constexpr int EPI_WARPS = MX && PAIR == 2 ? 8 : 4;
-  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  static constexpr int STG_BYTES = EPI_WARPS * 4096;   // epilogue staging (2 x 2 KB per warp)
-  static constexpr int FIXED_BYTES = STG_BYTES + 1024 /*align*/ + 256 /*bars*/ +
-                                     2 * (kMaxE + 1) * 4 + 512 /*row partials*/ + 64 + 256;
+  // Epilogue: groups of 4 warps (one per TMEM lane quarter).  Block-scaled
+  // tiles take half the MMA time of bf16 tiles of the same K, so they get two
+  // groups that take alternate tiles (each group owns one accumulator and
+  // has two tiles' worth of MMA time for its epilogue).
+  static constexpr int EPI_WARPS = 4;             // warps per group
+  static constexpr int EPI_GROUPS = MX ? 2 : 1;
+  // Block-scaled stages hold 384 tensor cycles of MMAs, less than one thread
+  // takes to issue a stage's three scale copies, four MMAs and commit, or
+  // its five TMA loads: the issue work is split over two more warps, one
+  // loading B and its scales, one copying the scales into tensor memory.
+  static constexpr bool SPLIT_ISSUE = MX;
+  static constexpr int EXTRA_WARPS = SPLIT_ISSUE ? 2 : 0;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS * EPI_GROUPS + 32 * EXTRA_WARPS;
+  static constexpr int STG_BYTES = EPI_WARPS * EPI_GROUPS * 4096;   // staging (2 x 2 KB per warp)
+  static constexpr int FIXED_BYTES = STG_BYTES + 1024 /*align*/ + 512 /*bars*/ +
+                                     2 * (kMaxE + 1) * 4 + kMaxE * 4 /*counts*/ + 64 + 256;
   static constexpr int STAGES_RAW = (232448 - FIXED_BYTES) / (STAGE_BYTES + SF_BYTES);
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-  // TMEM: NACC accumulators of BN columns; MXFP8 keeps one accumulator and a
-  // 16-column scale slot per pipeline stage from column 256 on.
-  static constexpr int NACC = MX ? 1 : 2;
-  static constexpr int SF_COL0 = 256;
+  // TMEM: two accumulators of BN columns (the epilogue of one tile overlaps
+  // the MMAs of the next); block-scaled runs add a 16-column scale slot per
+  // pipeline stage after them.
+  static constexpr int NACC = 2;
+  static constexpr int SF_COL0 = 2 * BN;
   static constexpr int TMEM_COLS = MX ? 512 : 2 * BN;
   static constexpr int KSTEPS = 4;                // MMAs per stage (32 bytes of K each)
   static constexpr int MN_KSTEP_BYTES = (32 / ES) * 128;  // MN-major advance per MMA
   static constexpr uint32_t FMT = ES == 2 ? 1u : (ES == 4 ? 2u : 0u);  // BF16 : TF32 : E4M3
   static constexpr int SF_REGION = (STAGES * SF_BYTES + 255) / 256 * 256;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STG_BYTES + SF_REGION +
-                                    1024 /*align*/ + 256 /*bars*/ + 2 * (kMaxE + 1) * 4 + 512 + 64;
+                                    1024 /*align*/ + 512 /*bars*/ + 2 * (kMaxE + 1) * 4 + kMaxE * 4 + 64;
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+  static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
   static_assert(!MX || SF_COL0 + STAGES * 16 <= 512, "TMEM scale slots");
-  // Block-scaled pairs: the last 128 columns hold, per lane quarter, the
-  // second half of both epilogue warps' columns (64 each), moved out of the
-  // accumulator so it can be released half-way through the gate/up and D
-  // epilogues.
-  static constexpr bool SPLIT = MX && PAIR == 2;
-  static constexpr int SPARE_COL = 384;
-  static_assert(!SPLIT || SF_COL0 + STAGES * 16 <= SPARE_COL, "TMEM spare columns");
 };
 
 // ------------------------------------------------------------ tile decode
@@ -178,6 +189,8 @@ __device__ __forceinline__ int last_le(const int* arr, int E, int v) {
 template <class C>
 __device__ __forceinline__ Tile decode_tile(const EngineParams& P, const int* cum, const int* s_po,
                                             const int* s_pt, int t, int rank) {
+  // s_pt and the per-expert row counts are consecutive arrays of kMaxE + 1
+  const int* s_cnt = s_pt + (kMaxE + 1);
   Tile ti;
   int p = 0;
   while (p + 1 < P.nprob && t >= cum[p + 1]) ++p;
@@ -195,7 +208,11 @@ __device__ __forceinline__ Tile decode_tile(const EngineParams& P, const int* cu
     ti.m0 = ti.mb * 128;
     ti.valid = ti.m0 < g.M;
     ti.kbase = s_po[ti.e];
-    ti.nk = (s_po[ti.e + 1] - s_po[ti.e]) / C::BK;
+    // K = the expert's rows; stages past its last real row would only add
+    // the zero pad rows, so the loop stops at the stage holding that row
+    const int rows_e = s_po[ti.e + 1] - s_po[ti.e];
+    const int cnt = s_cnt[ti.e];
+    ti.nk = (cnt >= 0 ? min(rows_e, (cnt + C::BK - 1) / C::BK * C::BK) : rows_e) / C::BK;
     ti.n0 = ti.ntile * C::BN;
   } else {
     const int q = lt / g.nt;
@@ -288,13 +305,15 @@ __device__ __forceinline__ void tma_load(void* dst, const CUtensorMap* m, int x,
 }
 
 // ----------------------------------------------------------------- roles
-// Producer (one thread per CTA).  With PAIR == 2 both CTAs load their own A
-// rows and their half of B into their own shared memory, and both signal the
-// leader CTA's full barrier, which the leader arms with the pair's bytes.
+// Producer (one thread per CTA, or two: `part` 0 loads A and its scales and
+// arms the full barrier, part 1 loads B and its scales; -1 loads all).  With
+// PAIR == 2 both CTAs load their own A rows and their half of B into their
+// own shared memory, and both signal the leader CTA's full barrier, which
+// the leader arms with the pair's bytes.
 template <class C>
 __device__ void producer_role(const EngineParams& P, const int* cum, int total, const int* s_po,
                               const int* s_pt, int rank, uint8_t* stages, uint8_t* sfreg,
-                              uint64_t* full, uint64_t* empty, const WaitCtl& wc) {
+                              uint64_t* full, uint64_t* empty, const WaitCtl& wc, int part) {
   int it = 0;
   const int cl = blockIdx.x / C::PAIR, ncl = gridDim.x / C::PAIR;
   // ready[nmb] counts every published (m-block, n-tile) of the signalling
@@ -321,7 +340,7 @@ __device__ void producer_role(const EngineParams& P, const int* cum, int total, 
     }
     // B column segments staged by this CTA: (first column or row, count)
     int seg0, seg1 = -1, seglen;
-    if (ti.kind == GK_FWD1) {
+    if (ti.kind == GK_FWD1 && !C::MX) {
       seglen = C::BN / 2;
       if (C::PAIR == 1) {
         seg0 = ti.n0;
@@ -330,8 +349,10 @@ __device__ void producer_role(const EngineParams& P, const int* cum, int total, 
         seg0 = rank ? g.I + ti.n0 : ti.n0;
       }
     } else {
+      // (block-scaled gate/up: W13's encoding interleaves 96 gate and 96 up
+      // columns per tile, so its B rows are contiguous like the others')
       seglen = C::BNL;
-      seg0 = ti.n0 + rank * C::BNL;
+      seg0 = ti.ntile * C::BN + rank * C::BNL;
     }
     bool ok = true;
     for (int kb = 0; kb < ti.nk; ++kb, ++it) {
@@ -342,10 +363,11 @@ __device__ void producer_role(const EngineParams& P, const int* cum, int total, 
       uint8_t* sB = sA + C::A_BYTES;
       uint32_t fbar = 0;
       if constexpr (C::PAIR == 2) fbar = mapa_shared(smem_u32(&full[s]), 0);
-      if (rank == 0) mbar_arrive_expect_tx(&full[s], C::TX_BYTES);
+      if (rank == 0 && part <= 0) mbar_arrive_expect_tx(&full[s], C::TX_BYTES);
       const int k0 = kb * C::BK;
       // A operand: M-major boxes (weight gradients) or one K-major box
-      if (g.a_mn) {
+      if (part == 1) {
+      } else if (g.a_mn) {
 #pragma unroll
         for (int j = 0; j < 128 / C::ATOM; ++j)
           tma_load<C>(sA + j * C::ATOM_BYTES, &g.tmA, ti.m0 + j * C::ATOM, ti.kbase + k0, &full[s],
@@ -356,7 +378,8 @@ __device__ void producer_role(const EngineParams& P, const int* cum, int total, 
       // B operand
       const int yrow = ti.kind == GK_DW ? 0 : ti.e * g.b_expert_rows;
       const int yb = ti.kind == GK_DW ? ti.kbase + k0 : ti.e * g.b_expert_rows + k0;
-      if (!g.b_mn) {
+      if (part == 0) {
+      } else if (!g.b_mn) {
         tma_load<C>(sB, &g.tmB, ti.kbase + k0, yrow + seg0, &full[s], fbar);
         if (seg1 >= 0)
           tma_load<C>(sB + seglen * 128, &g.tmB, ti.kbase + k0, yrow + seg1, &full[s], fbar);
@@ -371,31 +394,29 @@ __device__ void producer_role(const EngineParams& P, const int* cum, int total, 
       }
       if constexpr (C::MX) {
         // scale atoms: A's 128 rows x this K block (rows past the expert or
-        // M read atom 0: their results are dropped), then the atoms of every
-        // B column of the MMA -- for FWD1 the gate block, then the up block.
+        // M read atom 0: their results are dropped), then B's.
         uint8_t* sSFA = sfreg + s * C::SF_BYTES;
         uint8_t* sSFB = sSFA + C::SFA_BYTES;
         const int amb = ti.valid ? (ti.m0 >> 7) : 0;
-        tma_load<C>(sSFA, &g.tmSFA, 0, (amb * g.sfa_kg + ((ti.kbase + k0) >> 7)) * 4, &full[s],
-                    fbar);
-        const int kidx = g.b_mn ? yb : ti.kbase + k0;
-        const int nseg = ti.kind == GK_FWD1 ? 2 : 1;
-        int ai = 0;
-        for (int sg = 0; sg < nseg; ++sg) {
-          const int seg = ti.n0 + (sg ? g.I : 0);
-          for (int j = 0; j < C::BN / nseg / 128; ++j, ++ai) {
-            const int mn = (g.b_mn ? 0 : yrow) + seg + 128 * j;
-            tma_load<C>(sSFB + ai * 512, &g.tmSFB, 0, ((mn >> 7) * g.sfb_kg + (kidx >> 7)) * 4,
-                        &full[s], fbar);
-          }
-        }
+        if (part != 1)
+          tma_load<C>(sSFA, &g.tmSFA, 0, (amb * g.sfa_kg + ((ti.kbase + k0) >> 7)) * 4, &full[s],
+                      fbar);
+        // B (K-major): the two atoms of the tile's 192 columns
+        const int kidx = ti.kbase + k0;
+        const int64_t mn0 = (ti.kind == GK_DW ? 0 : (int64_t)ti.e * g.sfb_seg) + (int64_t)ti.ntile * 256;
+        if (part != 0)
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            tma_load<C>(sSFB + j * 512, &g.tmSFB, 0,
+                        (int)((((mn0 >> 7) + j) * g.sfb_kg + (kidx >> 7)) * 4), &full[s], fbar);
       }
     }
     if (!ok) break;
   }
   // Drain: the latest use of every stage must have landed before exit (the
-  // leader owns the full barriers, which also count the peer's bytes).
-  if (rank == 0) {
+  // leader owns the full barriers, which also count the peer's bytes and
+  // the other part's).
+  if (rank == 0 && part <= 0) {
     const int n = it < C::STAGES ? it : C::STAGES;
     for (int q = 1; q <= n; ++q) {
       const int u = it - q;
@@ -410,7 +431,7 @@ __device__ void mma_role(const EngineParams& P, const int* cum, int total, const
                          const int* s_pt, uint8_t* stages, uint8_t* sfreg, uint64_t* full,
                          uint64_t* empty,
                          uint64_t* tfull, uint64_t* tempty, uint64_t* drain, uint32_t tmem_base,
-                         const WaitCtl& wc) {
+                         uint64_t* sfready, const WaitCtl& wc) {
   int it = 0, acc = 0;
   const uint32_t sbase = smem_u32(stages);
   const int cl = blockIdx.x / C::PAIR, ncl = gridDim.x / C::PAIR;
@@ -438,13 +459,15 @@ __device__ void mma_role(const EngineParams& P, const int* cum, int total, const
     for (int kb = 0; kb < ti.nk; ++kb, ++it) {
       const int s = it % C::STAGES;
       if (!wait_bar_p<C>(&full[s], (it / C::STAGES) & 1, wc)) { ok = false; break; }
+      // block-scaled: the scale copier has put this stage's scales in TMEM
+      if (C::SPLIT_ISSUE && !wait_bar_p<C>(&sfready[s], (it / C::STAGES) & 1, wc)) { ok = false; break; }
       tc_fence_after();
       const uint32_t aA = sbase + s * C::STAGE_BYTES;
       const uint32_t aB = aA + C::A_BYTES;
       uint32_t sf_slot = 0;
-      if constexpr (C::MX) {
+      if constexpr (C::MX) sf_slot = tmem_base + C::SF_COL0 + s * 16;
+      if constexpr (C::MX && !C::SPLIT_ISSUE) {
         // scales of this stage into its TMEM slot: A at +0..3, B at +4..
-        sf_slot = tmem_base + C::SF_COL0 + s * 16;
         const uint32_t aS = smem_u32(sfreg) + s * C::SF_BYTES;
 #pragma unroll
         for (int j = 0; j < 1 + C::SFB_BYTES / 512; ++j) {
@@ -484,20 +507,59 @@ __device__ void mma_role(const EngineParams& P, const int* cum, int total, const
   wait_bar_drain(drain, 0, wc.limit_ns);
 }
 
+// Scale copier (block-scaled runs, one thread of the leader CTA): once a
+// stage's operands and scale atoms have landed, copies the scales into that
+// stage's TMEM slot (A at +0..3, B at +4..11) and signals sfready[stage]
+// when the copies have completed.  A slot is rewritten only after the stage
+// was refilled, i.e. after the MMAs that read its previous scales finished.
+template <class C>
+__device__ void sf_role(const EngineParams& P, const int* cum, int total, const int* s_po,
+                        const int* s_pt, uint8_t* sfreg, uint64_t* full, uint64_t* sfready,
+                        uint64_t* drain, uint32_t tmem_base, const WaitCtl& wc) {
+  int it = 0;
+  const int cl = blockIdx.x / C::PAIR, ncl = gridDim.x / C::PAIR;
+  for (int t = cl; t < total; t += ncl) {
+    const Tile ti = decode_tile<C>(P, cum, s_po, s_pt, t, 0);
+    bool ok = true;
+    for (int kb = 0; kb < ti.nk; ++kb, ++it) {
+      const int s = it % C::STAGES;
+      if (!wait_bar_p<C>(&full[s], (it / C::STAGES) & 1, wc)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t slot = tmem_base + C::SF_COL0 + s * 16;
+      const uint32_t aS = smem_u32(sfreg) + s * C::SF_BYTES;
+#pragma unroll
+      for (int j = 0; j < 1 + C::SFB_BYTES / 512; ++j) {
+        if constexpr (C::PAIR == 2)
+          tmem_cp_32x128b_x4_pair(slot + 4 * j, smem_desc_rows16(aS + 512 * j));
+        else
+          tmem_cp_32x128b_x4(slot + 4 * j, smem_desc_rows16(aS + 512 * j));
+      }
+      if constexpr (C::PAIR == 2) tc_commit_pair(&sfready[s], 1); else tc_commit(&sfready[s]);
+    }
+    if (!ok) break;
+  }
+  // every copy completed before TMEM is released
+  if constexpr (C::PAIR == 2) tc_commit_pair(drain, 1); else tc_commit(drain);
+  wait_bar_drain(drain, 0, wc.limit_ns);
+}
+
 // ------------------------------------------------------- epilogue helpers
-// MXFP8 encodings of a warp's 32 x 32 block of A (lane = row, v = its 32
-// columns from col0), from the bf16 values the stored A would hold, so the
-// codes equal those of the quantiser kernels on the stored tensor:
+// MXFP8 encodings of a warp's 32 x 32 block of a result (lane = row, v = its
+// 32 columns from col0), from the bf16 values the stored result would hold,
+// so the codes equal those of the quantiser kernels on the stored tensor:
 // row-wise (one 32-column block per lane) and, when qc is set, column-wise
 // (one 32-row block per column: the warp's rows lie in one expert's group,
-// whose padded start is a multiple of 128).  The column maxima go through
-// `tsm`, 4 KB of this warp's shared memory that no copy is reading: lane r
-// writes |v[i]| to word 32 r + (i ^ r), lane j reads column j (both without
-// bank conflicts), and the per-column factors return by shuffle.
+// whose padded start is a multiple of 128).  `tsm` is 4 KB of this warp's
+// shared memory that no copy is reading: lane r writes its values to word
+// 32 r + (i ^ r) and lane j reads column j (both without bank conflicts).
+// col_ld == 0: column-wise codes at [row][col] (an A operand, M-major);
+// col_ld > 0: stored transposed at [col][row] with row pitch col_ld and the
+// scales in the 192-column tile slots (a K-major B operand), each lane
+// encoding one column.
 __device__ __forceinline__ void encode_mx_block(float (&v)[32], int64_t row, int col0, int C,
                                                 uint8_t* qr, uint8_t* sr, uint8_t* qc,
                                                 uint8_t* sc, int64_t kg_rows, float* tsm,
-                                                int lane) {
+                                                int lane, int64_t col_ld = 0) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
   float am = 0.f;
@@ -515,6 +577,31 @@ __device__ __forceinline__ void encode_mx_block(float (&v)[32], int64_t row, int
   dr[1] = make_uint4(o[4], o[5], o[6], o[7]);
   sr[mma_scale_index(row, col0 >> 5, C >> 7)] = (uint8_t)sb;
   if (!qc) return;
+  if (col_ld > 0) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) tsm[lane * 32 + (i ^ lane)] = v[i];
+    __syncwarp();
+    float cv[32];                      // column col0 + lane, rows row0 .. row0 + 31
+    float cm = 0.f;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      cv[r] = tsm[r * 32 + (lane ^ r)];
+      cm = fmaxf(cm, fabsf(cv[r]));
+    }
+    __syncwarp();                      // reads done before the staging is reused
+    const int64_t row0 = row - lane;
+    const int sj = mx_scale_byte(cm);
+    sc[mma_scale_index(mx_tile_pos(col0 + lane), (int)(row0 >> 5), kg_rows)] = (uint8_t)sj;
+    const float invj = mx_inv_scale(sj);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      o[i] = (uint32_t)e4m3x2(cv[4 * i] * invj, cv[4 * i + 1] * invj) |
+             ((uint32_t)e4m3x2(cv[4 * i + 2] * invj, cv[4 * i + 3] * invj) << 16);
+    uint4* dc = reinterpret_cast<uint4*>(qc + (size_t)(col0 + lane) * col_ld + row0);
+    dc[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dc[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < 32; ++i) tsm[lane * 32 + (i ^ lane)] = fabsf(v[i]);
   __syncwarp();
@@ -580,9 +667,10 @@ __device__ __forceinline__ void load32(const Elt* src, float (&v)[32]) {
 __device__ __forceinline__ float sigmoid_f(float u) { return __fdividef(1.f, 1.f + __expf(-u)); }
 __device__ __forceinline__ float silu_f(float u) { return __fdividef(u, 1.f + __expf(-u)); }
 
+// Named barrier of one epilogue group (ids 1, 2, ...).
 template <int NTHREADS>
-__device__ __forceinline__ void epi_bar() {
-  asm volatile("bar.sync 1, %0;" ::"n"(NTHREADS) : "memory");
+__device__ __forceinline__ void epi_bar(int group) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "n"(NTHREADS) : "memory");
 }
 
 // Staging of bf16 results (per epilogue warp: two 2 KB buffers of 32 rows x
@@ -626,17 +714,18 @@ template <class C, typename Elt>
 __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, const int* s_po,
                               const int* s_pt, int rank, uint64_t* tfull, uint64_t* tempty,
                               uint32_t tmem_base, volatile int* s_go, uint8_t* stg,
-                              float* s_part, const WaitCtl& wc) {
+                              const WaitCtl& wc) {
   constexpr bool TS = sizeof(Elt) == 2;      // bf16 results leave through TMA stores
   constexpr int NV = 32 * (int)sizeof(Elt) / 16;   // 16-byte vectors per 32 elements
-  constexpr int ET = C::EPI_WARPS * 32;      // epilogue threads
-  constexpr int NH = C::EPI_WARPS / 4;       // column parts per tile row (1 or 2)
+  constexpr int ET = C::EPI_WARPS * 32;      // threads of an epilogue group
+  constexpr int NG = C::EPI_GROUPS;
+  static_assert(NG == 1 || NG == C::NACC, "one accumulator per epilogue group");
   const int ew = (threadIdx.x >> 5) - 2;     // epilogue warp
+  const int grp = ew / C::EPI_WARPS;         // its group: tiles acc with acc % NG == grp
   const int q = (threadIdx.x >> 5) & 3;      // TMEM lane quarter of this warp
-  const int h = ew >> 2;                     // column part of this warp
   const int lane = threadIdx.x & 31;
   const int r = q * 32 + lane;               // tile row of this thread
-  const bool leader = threadIdx.x == 64;     // first epilogue thread
+  const bool leader = threadIdx.x == 64 + grp * ET;   // first thread of the group
   const int cl = blockIdx.x / C::PAIR, ncl = gridDim.x / C::PAIR;
   uint8_t* sb0 = stg + ew * 4096;
   uint8_t* sb1 = sb0 + 2048;
@@ -656,15 +745,16 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
     fence_proxy_async_smem();
     __syncwarp();
   };
-  int acc = 0;
-  for (int t = cl; t < total; t += ncl) {
+  int acc = grp;   // this CTA's tile sequence index
+  for (int t = cl + grp * ncl; t < total; t += NG * ncl, acc += NG) {
     const Tile ti = decode_tile<C>(P, cum, s_po, s_pt, t, rank);
+    const int gs = grp * 2 + ((acc / NG) & 1);   // this group's decision slot
     const GemmProblem& g = P.prob[ti.p];
     const int buf = acc % C::NACC;
     const int yrow = ti.m0 + q * 32;         // first row of this warp's slice
     // accumulator columns [cb, cb + cw) of this warp (FWD1: of each half)
-    const int cw = (ti.kind == GK_FWD1 ? C::BN / 2 : C::BN) / NH;
-    const int cb = h * cw;
+    const int cw = ti.kind == GK_FWD1 ? C::BN / 2 : C::BN;
+    const int cb = 0;
     // dSwiGLU inputs: the first chunk of h13 is fetched before the wait
     uint4 pu[NV], pv[NV];
     const Elt* h13a = nullptr;
@@ -683,10 +773,10 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
     }
     // One thread waits; the decision is shared so all epilogue threads take
     // the same path through the named barriers below.  (s_go is indexed by
-    // acc & 1 so a slow reader never sees the next tile's decision.)
-    if (leader) s_go[acc & 1] = wait_bar_p<C>(&tfull[buf], (acc / C::NACC) & 1, wc) ? 1 : 0;
-    epi_bar<ET>();
-    if (!s_go[acc & 1]) break;
+    // the group's tile parity so a slow reader never sees the next decision.)
+    if (leader) s_go[gs] = wait_bar_p<C>(&tfull[buf], (acc / C::NACC) & 1, wc) ? 1 : 0;
+    epi_bar<ET>(grp);
+    if (!s_go[gs]) break;
     tc_fence_after();
     __syncwarp();
     const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * C::BN;
@@ -714,13 +804,6 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
         store32<Elt>(dst + 32, *reinterpret_cast<const float(*)[32]>(&y[32]));
       }
     };
-    bool released = false;
-    // gate/up and D on block-scaled pairs: the second half of this warp's
-    // columns is moved to the spare TMEM columns, and the accumulator is
-    // released once the first half has been read
-    auto spare_col = [&](int c) {
-      return tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(C::SPARE_COL + h * 64 + c);
-    };
     // gate of a tile row: 1 without a gate vector, 0 on pad rows
     auto row_gate = [&](const GemmProblem& gp, int row) -> float {
       if (!gp.gate) return 1.f;
@@ -731,69 +814,7 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       }
       return a >= 0 ? gp.gate[a] : 0.f;
     };
-    auto release_now = [&]() {
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(buf ? tempty_cl1 : tempty_cl0);
-      released = true;
-    };
-    if constexpr (C::EPI_WARPS == 8) {
-      // Block-scaled pairs hold their only accumulator until it is
-      // released: for the plain kinds the warp's 128 columns are read and
-      // packed to bf16 first, the accumulator is released, and the staging
-      // and bulk stores run while the next tile's MMAs do.
-      if (ti.kind == GK_FWD2 || ti.kind == GK_BWD_DX || ti.kind == GK_DW) {
-        const bool have = ti.valid && !(ti.kind == GK_DW && ti.nk == 0);   // CTA-uniform
-        const float gt = ti.kind == GK_FWD2 && ti.valid ? row_gate(g, ti.m0 + r) : 1.f;
-        uint32_t pk[64];
-        if (have) {
-          tmem_ld64(taddr + cb, x);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(x[2 * i] * gt, x[2 * i + 1] * gt);
-          tmem_ld64_after(taddr + cb + 64, x, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-#pragma unroll
-          for (int i = 0; i < 32; ++i) pk[32 + i] = pack_bf16(x[2 * i] * gt, x[2 * i + 1] * gt);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 64; ++i) pk[i] = 0u;
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(buf ? tempty_cl1 : tempty_cl0);
-        released = true;
-        if (ti.valid) {
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            stage_begin();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int rr = lane;
-              *reinterpret_cast<uint4*>(sb0 + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4)) =
-                  make_uint4(pk[32 * h2 + 4 * c + 0], pk[32 * h2 + 4 * c + 1],
-                             pk[32 * h2 + 4 * c + 2], pk[32 * h2 + 4 * c + 3]);
-              *reinterpret_cast<uint4*>(sb1 + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4)) =
-                  make_uint4(pk[32 * h2 + 16 + 4 * c + 0], pk[32 * h2 + 16 + 4 * c + 1],
-                             pk[32 * h2 + 16 + 4 * c + 2], pk[32 * h2 + 16 + 4 * c + 3]);
-            }
-            stage_end();
-            if (lane == 0) {
-              const int xc = ti.n0 + cb + 64 * h2;
-              if (ti.kind == GK_DW) {
-                tma_store_3d_ef(&g.tmO, sb0, xc, ti.m0 + q * 32, ti.e, pol_ef);
-                tma_store_3d_ef(&g.tmO, sb1, xc + 32, ti.m0 + q * 32, ti.e, pol_ef);
-              } else {
-                tma_store_2d_ef(&g.tmO, sb0, xc, yrow, pol_ef);
-                tma_store_2d_ef(&g.tmO, sb1, xc + 32, yrow, pol_ef);
-              }
-              bulk_commit();
-            }
-          }
-        }
-      }
-    }
-    if (released) {
-      // stored above, accumulator already released
-    } else if (!ti.valid) {
+    if (!ti.valid) {
       // rows past the tile's expert (odd m-block count) or past M: no output
     } else if (ti.kind == GK_FWD1) {
       const int row = ti.m0 + r;
@@ -802,16 +823,9 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       // with a gate vector the activation leaves as gate * A (0 on pad rows)
       const float ga = row_gate(g, row);
       const bool zrow = ga == 0.f;
-      const int half = cb + cw / 2;
-      if constexpr (C::SPLIT) tmem_move32x2(taddr + half, taddr + C::BN / 2 + half, spare_col(0));
 #pragma unroll 1
       for (int c = cb; c < cb + cw; c += 32) {
-        if (C::SPLIT && c >= half)
-          tmem_ld32x2(spare_col(c - half), spare_col(c - half + 32), v, w);
-        else
-          tmem_ld32x2(taddr + c, taddr + C::BN / 2 + c, v, w);   // u: gate half, v: up half
-        // the last accumulator chunk is in registers: release before its stores
-        if (C::SPLIT && c + 32 == half) release_now();
+        tmem_ld32x2(taddr + c, taddr + C::BN / 2 + c, v, w);   // u: gate half, v: up half
         if (h13) {
           if constexpr (TS) {
             stage_begin();
@@ -851,7 +865,7 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       const float gt = row_gate(g, row);
       Elt* out = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
 #pragma unroll 1
-      for (int c = cb; c < cb + cw; c += 64) {
+      for (int c = cb; c < cb + cw && ti.n0 + c < g.N; c += 64) {   // a last tile may be ragged
         tmem_ld64(taddr + c, x);
 #pragma unroll
         for (int i = 0; i < 64; ++i) x[i] *= gt;
@@ -867,27 +881,17 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       const float gt = a >= 0 ? g.gate[a] : 0.f;
       Elt* dh = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
       float part = 0.f;
-      const int half = cb + cw / 2;
-      if constexpr (C::SPLIT) tmem_move32x2(taddr + half, taddr + half + 32, spare_col(0));
       uint32_t src = taddr + cb;               // TMEM columns of the next chunk
 #pragma unroll 1
       for (int c = cb; c < cb + cw; c += 32, src += 32) {
         float D[32];
-        if constexpr (C::SPLIT) {
-          // D first: the last accumulator chunk is in registers, release
-          // before its math (this order also keeps the pair under its
-          // register cap)
-          if (c == half) src = spare_col(0);
-          tmem_ld32(src, D);
-          if (c + 32 == half) release_now();
-        }
         unpack_raw<Elt, NV>(pu, v);            // u of this chunk
         unpack_raw<Elt, NV>(pv, w);            // v of this chunk
         if (c + 32 < cb + cw) {                // fetch the next chunk while this one runs
           load_raw<Elt, NV>(h13a + c + 32, pu);
           load_raw<Elt, NV>(h13a + g.I + c + 32, pv);
         }
-        if constexpr (!C::SPLIT) tmem_ld32(src, D);
+        tmem_ld32(src, D);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float u = v[i], vv = w[i];
@@ -899,15 +903,17 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
           w[i] = a >= 0 ? dA * si : 0.f;                                  // dv
         }
         if (C::MX && g.enc_row_q) {
-          // block-scaled runs: dh13 leaves as its two MXFP8 encodings (the
-          // dX and dW13 operands), decided from the bf16 values a stored
-          // dh13 would hold
-          stage_begin();   // the staging becomes the column-maximum scratch
+          // block-scaled runs: dh13 leaves as its two MXFP8 encodings,
+          // decided from the bf16 values a stored dh13 would hold: row-wise
+          // (the dX GEMM's A) and column-wise along tokens, stored
+          // transposed (the dW13 GEMM's K-major B)
+          stage_begin();   // the staging becomes the encoder's scratch
           encode_mx_block(v, row, ti.n0 + c, 2 * g.I, g.enc_row_q, g.enc_row_sf, g.enc_col_q,
-                          g.enc_col_sf, g.enc_col_kg, reinterpret_cast<float*>(sb0), lane);
+                          g.enc_col_sf, g.enc_col_kg, reinterpret_cast<float*>(sb0), lane,
+                          g.enc_col_ld);
           encode_mx_block(w, row, g.I + ti.n0 + c, 2 * g.I, g.enc_row_q, g.enc_row_sf,
                           g.enc_col_q, g.enc_col_sf, g.enc_col_kg, reinterpret_cast<float*>(sb0),
-                          lane);
+                          lane, g.enc_col_ld);
         } else if constexpr (TS) {
           stage_begin();
           stage_bf16_row(sb0, lane, v);
@@ -923,19 +929,12 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
           store32<Elt>(dh + g.I + c, w);
         }
       }
-      if constexpr (NH == 2) {
-        // the second column part hands its sum to the first (fixed order)
-        if (h == 1) s_part[r] = part;
-        epi_bar<ET>();
-        if (h == 0) g.partial[(size_t)row * g.nt + ti.ntile] = a >= 0 ? part + s_part[r] : 0.f;
-      } else {
-        g.partial[(size_t)row * g.nt + ti.ntile] = a >= 0 ? part : 0.f;
-      }
+      g.partial[(size_t)row * g.nt + ti.ntile] = a >= 0 ? part : 0.f;
     } else if (ti.kind == GK_BWD_DX) {
       const int row = ti.m0 + r;
       Elt* out = static_cast<Elt*>(g.out) + (size_t)row * g.ld_out + ti.n0;
 #pragma unroll 1
-      for (int c = cb; c < cb + cw; c += 64) {
+      for (int c = cb; c < cb + cw && ti.n0 + c < g.N; c += 64) {
         tmem_ld64(taddr + c, x);
         emit64(x, out + c, ti.n0 + c, yrow, -1, true);
       }
@@ -943,7 +942,7 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       const bool valid = ti.m0 + r < g.M;
       Elt* out = static_cast<Elt*>(g.out) + ((size_t)ti.e * g.M + ti.m0 + r) * g.ld_out + ti.n0;
 #pragma unroll 1
-      for (int c = cb; c < cb + cw; c += 64) {
+      for (int c = cb; c < cb + cw && ti.n0 + c < g.N; c += 64) {
         if (ti.nk > 0) {
           tmem_ld64(taddr + c, x);
         } else {
@@ -954,13 +953,11 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
         emit64(x, out + c, ti.n0 + c, ti.m0 + q * 32, ti.e, valid);
       }
     }
-    if (!released) {
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (C::PAIR == 2) mbar_arrive_cluster(buf ? tempty_cl1 : tempty_cl0);
-        else mbar_arrive(&tempty[buf]);
-      }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      if constexpr (C::PAIR == 2) mbar_arrive_cluster(buf ? tempty_cl1 : tempty_cl0);
+      else mbar_arrive(&tempty[buf]);
     }
     if (g.signal && ti.valid) {
       // Publish this tile's rows to TMA readers in other CTAs: the bulk
@@ -969,13 +966,12 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
       __syncwarp();
       fence_proxy_async_global();
       __threadfence();
-      epi_bar<ET>();
+      epi_bar<ET>(grp);
       if (leader) {
         red_release_add(P.ready + ti.mb, 1);
         red_release_add(P.ready + P.ready_all_index, 1);
       }
     }
-    ++acc;
   }
   if (TS && lane == 0) bulk_wait_all();    // every store done before the CTA exits
   __syncwarp();
@@ -997,12 +993,14 @@ __global__ void __launch_bounds__(Cfg<In, BN, PAIR>::THREADS, 1)
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sfready = drain + 1;        // [STAGES] (block-scaled runs)
+  uint64_t* drain2 = sfready + C::STAGES;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain2 + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
-  int* s_go = abort_flag + 1;           // [2]
-  int* s_po = reinterpret_cast<int*>(sfreg + C::SF_REGION + 256);
+  int* s_go = abort_flag + 1;           // [2 per epilogue group]
+  int* s_po = reinterpret_cast<int*>(sfreg + C::SF_REGION + 512);   // after the barriers
   int* s_pt = s_po + (kMaxE + 1);       // pair tiles before expert e (PAIR == 2)
-  float* s_part = reinterpret_cast<float*>(s_pt + (kMaxE + 1));   // [128] row partials
+  int* s_cnt = s_pt + (kMaxE + 1);      // rows of each expert (weight-gradient K)
 
   const int warp = threadIdx.x >> 5;
   const int rank = PAIR == 2 ? (int)cluster_ctarank() : 0;
@@ -1013,14 +1011,17 @@ __global__ void __launch_bounds__(Cfg<In, BN, PAIR>::THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], C::EPI_WARPS * PAIR);  // one arrival per epilogue warp of the pair
+      mbar_init(&tempty[b], C::EPI_WARPS * PAIR);  // one arrival per warp of the group, both CTAs
     }
     mbar_init(drain, 1);
+    for (int st = 0; st < C::STAGES; ++st) mbar_init(&sfready[st], 1);
+    mbar_init(drain2, 1);
     *abort_flag = 0;
-    s_go[0] = s_go[1] = 0;
+    for (int i = 0; i < 2 * C::EPI_GROUPS; ++i) s_go[i] = 0;
     fence_barrier_init();
   }
   for (int i = threadIdx.x; i <= P.E; i += blockDim.x) s_po[i] = P.padded_offsets[i];
+  for (int i = threadIdx.x; i < P.E; i += blockDim.x) s_cnt[i] = P.counts ? P.counts[i] : -1;
   if (warp == 1) {
     if constexpr (PAIR == 2) tmem_alloc_pair(tmem_holder, C::TMEM_COLS);
     else tmem_alloc(tmem_holder, C::TMEM_COLS);
@@ -1080,18 +1081,27 @@ __global__ void __launch_bounds__(Cfg<In, BN, PAIR>::THREADS, 1)
   const int total = cum[P.nprob];
   const WaitCtl wc{abort_flag, P.status, P.wait_ns};
 
+  constexpr int EPI_END = 2 + C::EPI_WARPS * C::EPI_GROUPS;   // first warp after the epilogue
   if (warp == 0) {
     if ((threadIdx.x & 31) == 0)
-      producer_role<C>(P, cum, total, s_po, s_pt, rank, stages, sfreg, full, empty, wc);
+      producer_role<C>(P, cum, total, s_po, s_pt, rank, stages, sfreg, full, empty, wc,
+                       C::SPLIT_ISSUE ? 0 : -1);
     __syncwarp();
   } else if (warp == 1) {
     if ((threadIdx.x & 31) == 0 && rank == 0)
       mma_role<C>(P, cum, total, s_po, s_pt, stages, sfreg, full, empty, tfull, tempty, drain,
-                  tmem_base, wc);
+                  tmem_base, sfready, wc);
+    __syncwarp();
+  } else if (warp < EPI_END) {
+    epilogue_role<C, Out>(P, cum, total, s_po, s_pt, rank, tfull, tempty, tmem_base, s_go, stg, wc);
+  } else if (warp == EPI_END) {
+    if ((threadIdx.x & 31) == 0)
+      producer_role<C>(P, cum, total, s_po, s_pt, rank, stages, sfreg, full, empty, wc, 1);
     __syncwarp();
   } else {
-    epilogue_role<C, Out>(P, cum, total, s_po, s_pt, rank, tfull, tempty, tmem_base, s_go, stg,
-                          s_part, wc);
+    if ((threadIdx.x & 31) == 0 && rank == 0)
+      sf_role<C>(P, cum, total, s_po, s_pt, sfreg, full, sfready, drain2, tmem_base, wc);
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -1267,6 +1277,7 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
   P.nprob = L.nprob;
   P.E = L.E;
   P.padded_offsets = L.padded_offsets;
+  P.counts = L.counts;
   P.ready = L.ready;
   P.ready_target = L.ready_target;
   P.ready_all_index = (int)((L.max_rows + 127) / 128);
@@ -1312,6 +1323,8 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
     g.enc_col_q = d.enc_col_q;
     g.enc_col_sf = d.enc_col_sf;
     g.enc_col_kg = d.enc_col_kg;
+    g.enc_col_ld = d.enc_col_ld;
+    g.sfb_seg = d.sfb_seg;
     if (es == 1 && !(make_tmap_sf(&g.tmSFA, d.sfa, d.sfa_bytes) &&
                      make_tmap_sf(&g.tmSFB, d.sfb, d.sfb_bytes))) {
       *st = MOE_ERR_INVALID_ARG;
@@ -1321,15 +1334,19 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
     const bool b_mn = d.b_mn != 0;
     if ((a_mn || b_mn) && es == 4) { *st = MOE_ERR_UNSUPPORTED; return cudaSuccess; }  // TF32: K-major only
     if (a_mn && d.kind != GK_DW) { *st = MOE_ERR_UNSUPPORTED; return cudaSuccess; }
+    if (b_mn && es == 1) { *st = MOE_ERR_UNSUPPORTED; return cudaSuccess; }  // 192-wide tiles: K-major B
     const int n_per_tile = d.kind == GK_FWD1 ? L.BN / 2 : L.BN;
     const int n_total = d.kind == GK_FWD1 ? d.N / 2 : d.N;
-    if (n_total % n_per_tile != 0) { *st = MOE_ERR_UNSUPPORTED; return cudaSuccess; }
-    g.nt = n_total / n_per_tile;
+    // the gate/up and D epilogues need whole tiles; the others store through
+    // views that clip a ragged last tile
+    const bool whole = d.kind == GK_FWD1 || d.kind == GK_BWD_D;
+    if (n_total % n_per_tile != 0 && (whole || es != 1)) { *st = MOE_ERR_UNSUPPORTED; return cudaSuccess; }
+    g.nt = (n_total + n_per_tile - 1) / n_per_tile;
     bool ok = a_mn ? make_tmap(&g.tmA, d.a, es, d.a_rows, d.a_cols, ATOM, BK)
                    : make_tmap(&g.tmA, d.a, es, d.a_rows, d.a_cols, BK, 128);
     ok = ok && (b_mn ? make_tmap(&g.tmB, d.b, es, d.b_rows, d.b_cols, ATOM, BK)
                      : make_tmap(&g.tmB, d.b, es, d.b_rows, d.b_cols, BK,
-                                 d.kind == GK_FWD1 ? L.BN / 2 : L.BN / pair));
+                                 d.kind == GK_FWD1 && es != 1 ? L.BN / 2 : L.BN / pair));
     if (es != 4) {   // bf16 results: bulk-store views of the outputs
       // every bf16 result leaves through a view built here; the results
       // that may be absent are FWD1's A and BWD_D's dh13 when the epilogue
@@ -1361,8 +1378,9 @@ cudaError_t launch_engine(const EngineLaunch& L, cudaStream_t s, moe_status* st)
       case 64: return launch_typed<__nv_bfloat16, __nv_bfloat16, 64, 1>(P, tile_bound, gang, s);
     }
   } else if (es == 1) {   // MXFP8 operands, bf16 outputs
-    if (L.BN == 256 && pair == 2) return launch_typed<uint8_t, __nv_bfloat16, 256, 2>(P, tile_bound, gang, s);
-    if (L.BN == 256) return launch_typed<uint8_t, __nv_bfloat16, 256, 1>(P, tile_bound, gang, s);
+    if (L.BN == kMxTileN && pair == 2)
+      return launch_typed<uint8_t, __nv_bfloat16, kMxTileN, 2>(P, tile_bound, gang, s);
+    if (L.BN == kMxTileN) return launch_typed<uint8_t, __nv_bfloat16, kMxTileN, 1>(P, tile_bound, gang, s);
   } else if (es == 4) {
     switch (L.BN) {
       case 256: return launch_typed<float, float, 256, 1>(P, tile_bound, gang, s);

@@ -68,9 +68,26 @@ struct DualGather {
   const float* gate;     // optional
   int32_t* status;
 };
+// Output forms for the block-scaled GEMMs' B operands (192-column tiles,
+// K-major B):
+//   row_seg > 0   row-wise scales in the 192-column tile slots of segments of
+//                 row_seg rows (mx_tile_slot), e.g. W2 [E*I, H] with I;
+//   col_ld > 0    column-wise codes stored transposed: column c of input
+//                 row r goes to row (r / col_seg) * C + perm(c), column
+//                 r % col_seg, of a [.., col_ld] byte matrix (col_seg, a
+//                 multiple of 128, is the K extent per segment), scales in
+//                 the tile slots of that row; col_perm 1 interleaves 96
+//                 gate and 96 up columns per tile (W13 for the gate/up GEMM).
+// qr == nullptr skips the row-wise output.
+struct DualOut {
+  int64_t row_seg;
+  int64_t col_ld, col_seg;
+  int col_perm;
+};
 cudaError_t launch_quantize_dual(const void* src, int R, int C, int ld, const int32_t* rows_dev,
                                  uint8_t* qr, uint8_t* sr, uint8_t* qc, uint8_t* sc,
-                                 cudaStream_t s, const DualGather* gather = nullptr);
+                                 cudaStream_t s, const DualGather* gather = nullptr,
+                                 const DualOut* out = nullptr);
 
 // gemm.cu
 struct GemmDesc {
@@ -100,10 +117,12 @@ struct GemmDesc {
   uint8_t* enc_col_q;
   uint8_t* enc_col_sf;
   int64_t enc_col_kg;          //   128-row groups of the column-wise scale atoms
+  int64_t enc_col_ld;          //   > 0: column-wise codes transposed ([col][row], this pitch)
   const uint8_t* sfa;          // MXFP8: scale atoms of A / B (quant.cu layout 1)
   const uint8_t* sfb;
   int64_t sfa_bytes, sfb_bytes;  // size of each scale-atom array (multiple of 512)
   int sfa_kg, sfb_kg;          // K groups of 128 in each operand's 2-D view
+  int64_t sfb_seg;             // B scale atoms: MN slots per expert segment (0: one segment)
 };
 
 struct EngineLaunch {
@@ -113,6 +132,7 @@ struct EngineLaunch {
   int elem_bytes;              // 2: bf16 (kind::f16), 4: fp32 (kind::tf32), 1: MXFP8
   int BN;                      // 64, 128 or 256
   const int32_t* padded_offsets;
+  const int32_t* counts;       // rows per expert (optional)
   int64_t max_rows;
   int32_t* ready;              // [(max_rows + 127) / 128 + 1] readiness counters
   int ready_target;

@@ -6,6 +6,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "mx_encode.cuh"
 
 namespace moe {
 
@@ -106,9 +107,14 @@ int64_t max_rows(const moe_dims* d) { return (int64_t)d->T * d->top_k + (int64_t
 
 bool aligned16(const void* p) { return p && ((uintptr_t)p & 15) == 0; }
 
+// The block-scaled GEMMs run 192-column tiles (96 gate + 96 up columns for
+// the gate/up GEMM) and stages of 128 K elements: I (an N of the gate/up
+// and D GEMMs, the K of the down GEMM) a multiple of 384, H of 128.
+bool mx_shape_ok(const moe_dims* d) { return d->I % 384 == 0 && d->H % 128 == 0; }
+
 // Tile width of the forward gate/up GEMM: BN/2 columns of each half per tile.
 int bn_fwd1(const moe_dims* d) {
-  if (mx_fwd(d)) return d->I % 256 == 0 && d->H % 256 == 0 ? 256 : 0;
+  if (mx_fwd(d)) return mx_shape_ok(d) ? kMxTileN : 0;
   const int atom = 128 / elem_bytes(d);
   for (int bn : {256, 128, 64})
     if (bn / 2 >= atom && d->I % (bn / 2) == 0) return bn;
@@ -120,7 +126,7 @@ int bn_div(int n) {
   return 0;
 }
 int bn_bwd(const moe_dims* d) {
-  if (mx_bwd(d)) return d->I % 256 == 0 && d->H % 256 == 0 ? 256 : 0;
+  if (mx_bwd(d)) return mx_shape_ok(d) ? kMxTileN : 0;
   for (int bn : {256, 128, 64})
     if (d->I % bn == 0 && d->H % bn == 0) return bn;
   return 0;
@@ -141,7 +147,8 @@ struct MxBuf {
   size_t q, sf, sf_bytes;
 };
 int64_t rows_pad(const moe_dims* d) { return (max_rows(d) + 127) / 128 * 128; }
-// codes of an [R, C] operand (R padded to 128 for the atoms)
+// codes of an [R, C] byte matrix (K = C) and the scale atoms of Rp MN slots
+// (R padded to 128, or the 192-column tile slots of a B operand)
 MxBuf mx_carve(size_t& o, size_t R, size_t Rp, size_t C) {
   MxBuf b;
   b.q = o;
@@ -166,11 +173,13 @@ FwdWs fwd_ws(const moe_dims* d) {
   w.w13t = o; o += t ? align256(2 * wsz) : 0;
   w.w2t = o; o += t ? align256(wsz) : 0;
   if (mx_fwd(d)) {
-    const size_t rp = (size_t)rows_pad(d), EH = (size_t)d->E * d->H, EI = (size_t)d->E * d->I;
-    w.x = mx_carve(o, rows, rp, d->H);
-    w.w13 = mx_carve(o, EH, EH, 2 * (size_t)d->I);
-    w.a = mx_carve(o, rows, rp, d->I);
-    w.w2 = mx_carve(o, EI, EI, d->H);
+    const size_t rp = (size_t)rows_pad(d), E = d->E, H = d->H, I = d->I;
+    w.x = mx_carve(o, rows, rp, H);
+    // B operands, K-major: W13 transposed [E*2I, H] (gate / up interleaved per
+    // tile) and W2 transposed [E*H, I]
+    w.w13 = mx_carve(o, E * 2 * I, E * mx_tile_slots(2 * I), H);
+    w.a = mx_carve(o, rows, rp, I);
+    w.w2 = mx_carve(o, E * H, E * mx_tile_slots(H), I);
   }
   w.total = o;
   return w;
@@ -204,16 +213,17 @@ BwdWs bwd_ws(const moe_dims* d) {
   w.xp_t = o; o += t ? align256(lt * d->H) : 0;
   w.dh13_t = o; o += t ? align256(lt * 2 * d->I) : 0;
   if (mx_bwd(d)) {
-    const size_t rp = (size_t)rows_pad(d), EH = (size_t)d->E * d->H, EI = (size_t)d->E * d->I;
-    const size_t H = d->H, I = d->I;
+    const size_t rp = (size_t)rows_pad(d), E = d->E, H = d->H, I = d->I;
     w.dy = mx_carve(o, rows, rp, H);
-    w.dygc = mx_carve(o, rows, rp, H);
+    // B operands of the weight gradients, K-major: gate * dY and dh13
+    // quantised along tokens, stored transposed ([H, rp], [2I, rp])
+    w.dygc = mx_carve(o, H, mx_tile_slots(H), rp);
     w.dh13r = mx_carve(o, rows, rp, 2 * I);
-    w.dh13c = mx_carve(o, rows, rp, 2 * I);
+    w.dh13c = mx_carve(o, 2 * I, mx_tile_slots(2 * I), rp);
     if (d->mode != MOE_MXFP8) {   // mxfp8: the forward leaves these in `saved`
-      w.w2r = mx_carve(o, EI, EI, H);
+      w.w2r = mx_carve(o, E * I, E * mx_tile_slots(I), H);
       w.actc = mx_carve(o, rows, rp, I);
-      w.w13r = mx_carve(o, EH, EH, 2 * I);
+      w.w13r = mx_carve(o, E * H, E * mx_tile_slots(H), 2 * I);
       w.xpc = mx_carve(o, rows, rp, H);
     }
   }
@@ -247,9 +257,10 @@ moe_saved_layout saved_layout(const moe_dims* d) {
   // forward workspace's row-wise copy)
   s.act = o; o += d->mode == MOE_MXFP8 ? 0 : align256(rows * d->I * es);
   if (d->mode == MOE_MXFP8) {
-    const size_t rp = (size_t)rows_pad(d), EH = (size_t)d->E * d->H, EI = (size_t)d->E * d->I;
-    const MxBuf x = mx_carve(o, rows, rp, d->H), a = mx_carve(o, rows, rp, d->I);
-    const MxBuf w13 = mx_carve(o, EH, EH, 2 * (size_t)d->I), w2 = mx_carve(o, EI, EI, d->H);
+    const size_t rp = (size_t)rows_pad(d), E = d->E, H = d->H, I = d->I;
+    const MxBuf x = mx_carve(o, rows, rp, H), a = mx_carve(o, rows, rp, I);
+    const MxBuf w13 = mx_carve(o, E * H, E * mx_tile_slots(H), 2 * I);
+    const MxBuf w2 = mx_carve(o, E * I, E * mx_tile_slots(I), H);
     s.x_col_q = x.q; s.x_col_sf = x.sf;
     s.act_col_q = a.q; s.act_col_sf = a.sf;
     s.w13_row_q = w13.q; s.w13_row_sf = w13.sf;
@@ -292,33 +303,35 @@ Mx mx_at(char* base, const MxBuf& b) {
   return Mx{base + b.q, reinterpret_cast<const uint8_t*>(base + b.sf), (int64_t)b.sf_bytes};
 }
 
-cudaError_t quant_rows(const void* src, int64_t R, int C, const Mx& m, int32_t* st, cudaStream_t s) {
-  return launch_quantize(src, (int)R, C, C, 1, nullptr, 0, (uint8_t*)m.q, (uint8_t*)m.sf, st, s, 1);
-}
 cudaError_t quant_cols(const void* src, int64_t R, int C, const int32_t* go, int G, const Mx& m,
                        int32_t* st, cudaStream_t s) {
   return launch_quantize(src, (int)R, C, C, 0, go, G, (uint8_t*)m.q, (uint8_t*)m.sf, st, s, 1);
 }
-// row-wise into `rw` and column-wise into `cw` (if given) from one read;
-// rows at or past *rows_dev (if given) untouched; with `g`, rows are gathered
-// token rows of src (see DualGather)
-cudaError_t quant_both(const void* src, int64_t R, int C, const int32_t* rows_dev, const Mx& rw,
-                       const Mx* cw, cudaStream_t s, const DualGather* g = nullptr) {
-  return launch_quantize_dual(src, (int)R, C, C, rows_dev, (uint8_t*)rw.q, (uint8_t*)rw.sf,
-                              cw ? (uint8_t*)cw->q : nullptr, cw ? (uint8_t*)cw->sf : nullptr, s, g);
+// One read of a bf16 [R, C] tensor, two encodings: row-wise into `rw` (if
+// given; `row_seg` > 0 puts its scales in the 192-column tile slots of a B
+// operand with segments of row_seg rows) and column-wise into `cw` (if
+// given; `col` says whether it is stored transposed for a K-major B).  Rows
+// at or past *rows_dev (if given) are untouched; with `g`, rows are gathered
+// token rows of src (see DualGather).
+cudaError_t quant_both(const void* src, int64_t R, int C, const int32_t* rows_dev, const Mx* rw,
+                       const Mx* cw, cudaStream_t s, const DualGather* g = nullptr,
+                       const DualOut& out = DualOut{}) {
+  return launch_quantize_dual(src, (int)R, C, C, rows_dev, rw ? (uint8_t*)rw->q : nullptr,
+                              rw ? (uint8_t*)rw->sf : nullptr, cw ? (uint8_t*)cw->q : nullptr,
+                              cw ? (uint8_t*)cw->sf : nullptr, s, g, &out);
 }
 // the backward's operands that the mxfp8 forward writes into `saved`
 struct MxSaved {
   Mx x_col, act_col, w13_row, w2_row;
 };
 MxSaved mx_saved(const moe_dims* d, const moe_saved_layout& sl, char* sv) {
-  const int64_t rp = rows_pad(d), EH = (int64_t)d->E * d->H, EI = (int64_t)d->E * d->I;
+  const int64_t rp = rows_pad(d), E = d->E, H = d->H, I = d->I;
   auto at = [&](size_t q, size_t sf, int64_t sf_bytes) {
     return Mx{sv + q, reinterpret_cast<const uint8_t*>(sv + sf), sf_bytes};
   };
-  return MxSaved{at(sl.x_col_q, sl.x_col_sf, rp * d->H / 32), at(sl.act_col_q, sl.act_col_sf, rp * d->I / 32),
-                 at(sl.w13_row_q, sl.w13_row_sf, EH * 2 * d->I / 32),
-                 at(sl.w2_row_q, sl.w2_row_sf, EI * d->H / 32)};
+  return MxSaved{at(sl.x_col_q, sl.x_col_sf, rp * H / 32), at(sl.act_col_q, sl.act_col_sf, rp * I / 32),
+                 at(sl.w13_row_q, sl.w13_row_sf, E * mx_tile_slots(H) * 2 * I / 32),
+                 at(sl.w2_row_q, sl.w2_row_sf, E * mx_tile_slots(I) * H / 32)};
 }
 
 // With save_for_backward, each quantisation pass also writes the backward's
@@ -326,7 +339,8 @@ MxSaved mx_saved(const moe_dims* d, const moe_saved_layout& sl, char* sv) {
 // The dispatch gather is fused into the first quantisation: X_perm exists
 // only as its MXFP8 encodings (saved x_perm is not stored in this mode); the
 // gate/up epilogue writes A's two encodings itself (A is never stored in
-// bf16 in this mode).
+// bf16 in this mode).  B operands are K-major: W13 and W2 are encoded
+// transposed (their K = H or I runs along the rows of the stored matrices).
 moe_status forward_mx(const moe_dims* d, const void* X, const void* W13, const void* W2,
                       const moe_route_out* r, void* h13, void* zg, char* wsb,
                       const FwdWs& w, const MxSaved& sv, int32_t* dev_status, cudaStream_t s) {
@@ -336,20 +350,19 @@ moe_status forward_mx(const moe_dims* d, const void* X, const void* W13, const v
   const int32_t* tpad = r->padded_offsets + E;
   const bool both = d->save_for_backward != 0;
   const DualGather gx{r->assign_of_row, d->top_k, d->T * d->top_k, nullptr, dev_status};
-  MOE_TRY(quant_both(X, rows, H, tpad, x, both ? &sv.x_col : nullptr, s, &gx));
-  if (both) {
-    MOE_TRY(quant_both(W13, (int64_t)E * H, 2 * I, nullptr, sv.w13_row, &w13, s));
-  } else {
-    MOE_TRY(quant_cols(W13, (int64_t)E * H, 2 * I, nullptr, 0, w13, dev_status, s));
-  }
+  MOE_TRY(quant_both(X, rows, H, tpad, &x, both ? &sv.x_col : nullptr, s, &gx));
+  // W13: row-wise for dX (saved), transposed column-wise for the gate/up GEMM
+  MOE_TRY(quant_both(W13, (int64_t)E * H, 2 * I, nullptr, both ? &sv.w13_row : nullptr, &w13, s,
+                     nullptr, DualOut{H, H, H, 1}));
   moe_status st;
   EngineLaunch L;
   memset(&L, 0, sizeof(L));
   L.nprob = 1;
   L.E = E;
   L.elem_bytes = 1;
-  L.BN = 256;
+  L.BN = kMxTileN;
   L.padded_offsets = r->padded_offsets;
+  L.counts = r->counts;
   L.max_rows = rows;
   L.status = dev_status;
   L.wait_ns = wait_limit_ns();
@@ -358,9 +371,8 @@ moe_status forward_mx(const moe_dims* d, const void* X, const void* W13, const v
     g = GemmDesc{};
     g.kind = GK_FWD1;
     g.a = x.q; g.a_rows = rows; g.a_cols = H; g.sfa = x.sf; g.sfa_bytes = x.sf_bytes; g.sfa_kg = H / 128;
-    g.b_mn = 1;
-    g.b = w13.q; g.b_rows = (int64_t)E * H; g.b_cols = 2 * I; g.b_expert_rows = H;
-    g.sfb = w13.sf; g.sfb_bytes = w13.sf_bytes; g.sfb_kg = (int)((int64_t)E * H / 128);
+    g.b = w13.q; g.b_rows = (int64_t)E * 2 * I; g.b_cols = H; g.b_expert_rows = 2 * I;
+    g.sfb = w13.sf; g.sfb_bytes = w13.sf_bytes; g.sfb_kg = H / 128; g.sfb_seg = mx_tile_slots(2 * I);
     g.N = 2 * I; g.K = H; g.I = I;
     // A leaves the epilogue as its MXFP8 encodings (row-wise for the down
     // GEMM, column-wise along tokens for dW2), never as bf16
@@ -373,19 +385,16 @@ moe_status forward_mx(const moe_dims* d, const void* X, const void* W13, const v
     MOE_TRY(launch_engine(L, s, &st));
     if (st != MOE_OK) return st;
   }
-  if (both) {
-    MOE_TRY(quant_both(W2, (int64_t)E * I, H, nullptr, sv.w2_row, &w2, s));
-  } else {
-    MOE_TRY(quant_cols(W2, (int64_t)E * I, H, nullptr, 0, w2, dev_status, s));
-  }
+  // W2: row-wise for D (saved), transposed column-wise for the down GEMM
+  MOE_TRY(quant_both(W2, (int64_t)E * I, H, nullptr, both ? &sv.w2_row : nullptr, &w2, s, nullptr,
+                     DualOut{I, I, I, 0}));
   {
     GemmDesc& g = L.prob[0];
     g = GemmDesc{};
     g.kind = GK_FWD2;
     g.a = a.q; g.a_rows = rows; g.a_cols = I; g.sfa = a.sf; g.sfa_bytes = a.sf_bytes; g.sfa_kg = I / 128;
-    g.b_mn = 1;
-    g.b = w2.q; g.b_rows = (int64_t)E * I; g.b_cols = H; g.b_expert_rows = I;
-    g.sfb = w2.sf; g.sfb_bytes = w2.sf_bytes; g.sfb_kg = (int)((int64_t)E * I / 128);
+    g.b = w2.q; g.b_rows = (int64_t)E * H; g.b_cols = I; g.b_expert_rows = H;
+    g.sfb = w2.sf; g.sfb_bytes = w2.sf_bytes; g.sfb_kg = I / 128; g.sfb_seg = mx_tile_slots(H);
     g.N = H; g.K = I;
     g.out = zg; g.ld_out = H;
     g.gate = r->gate; g.assign_of_row = r->assign_of_row; g.n_assign = d->T * d->top_k;
@@ -399,7 +408,8 @@ moe_status forward_mx(const moe_dims* d, const void* X, const void* W13, const v
 // writes dh13's two encodings, which dX and dW13 read, so the gradient GEMMs
 // run as two launches: {D + dSwiGLU, dW2}, then {dX, dW13}.
 // The dY gather is fused into its quantisation: dY_perm and gate * dY_perm
-// exist only as their MXFP8 encodings.
+// exist only as their MXFP8 encodings.  The weight gradients' B operands
+// (gate * dY and dh13 along tokens) are stored transposed (K-major).
 moe_status backward_mx(const moe_dims* d, const void* dY, const void* W13, const void* W2,
                        const moe_route_out* r, const void* x_perm, const void* h13,
                        const void* act, void* dxp,
@@ -419,17 +429,18 @@ moe_status backward_mx(const moe_dims* d, const void* dY, const void* W13, const
   const Mx xpc = saved_mx ? sv.x_col : mx_at(wsb, w.xpc);
   const int32_t* po = r->padded_offsets;
   const DualGather gy{r->assign_of_row, d->top_k, d->T * d->top_k, r->gate, dev_status};
-  MOE_TRY(quant_both(dY, rows, H, po + E, dy, &dygc, s, &gy));
+  MOE_TRY(quant_both(dY, rows, H, po + E, &dy, &dygc, s, &gy, DualOut{0, rp, rp, 0}));
   if (!saved_mx) {
-    MOE_TRY(quant_rows(W2, (int64_t)E * I, H, w2r, dev_status, s));
+    MOE_TRY(quant_both(W2, (int64_t)E * I, H, nullptr, &w2r, nullptr, s, nullptr, DualOut{I, 0, 0, 0}));
     MOE_TRY(quant_cols(act, rows, I, po, E, actc, dev_status, s));
   }
   EngineLaunch L;
   memset(&L, 0, sizeof(L));
   L.E = E;
   L.elem_bytes = 1;
-  L.BN = 256;
+  L.BN = kMxTileN;
   L.padded_offsets = po;
+  L.counts = r->counts;
   L.max_rows = rows;
   L.status = dev_status;
   L.wait_ns = wait_limit_ns();
@@ -441,29 +452,30 @@ moe_status backward_mx(const moe_dims* d, const void* dY, const void* W13, const
     gd.kind = GK_BWD_D;
     gd.a = dy.q; gd.a_rows = rows; gd.a_cols = H; gd.sfa = dy.sf; gd.sfa_bytes = dy.sf_bytes; gd.sfa_kg = H / 128;
     gd.b = w2r.q; gd.b_rows = (int64_t)E * I; gd.b_cols = H; gd.b_expert_rows = I;
-    gd.sfb = w2r.sf; gd.sfb_bytes = w2r.sf_bytes; gd.sfb_kg = H / 128;
+    gd.sfb = w2r.sf; gd.sfb_bytes = w2r.sf_bytes; gd.sfb_kg = H / 128; gd.sfb_seg = mx_tile_slots(I);
     gd.N = I; gd.K = H; gd.I = I;
     // dh13 leaves the dSwiGLU epilogue as its two MXFP8 encodings (row-wise
-    // for dX, column-wise along tokens for dW13), never as bf16
+    // for dX, column-wise along tokens, transposed, for dW13), never as bf16
     gd.enc_row_q = (uint8_t*)dh13r.q; gd.enc_row_sf = (uint8_t*)dh13r.sf;
     gd.enc_col_q = (uint8_t*)dh13c.q; gd.enc_col_sf = (uint8_t*)dh13c.sf;
-    gd.enc_col_kg = rp / 128;
+    gd.enc_col_kg = rp / 128; gd.enc_col_ld = rp;
     gd.aux = h13; gd.ld_aux = 2 * I;
     gd.gate = r->gate; gd.assign_of_row = r->assign_of_row; gd.n_assign = d->T * d->top_k;
     gd.partial = partial;
     GemmDesc& gw2 = L.prob[1];
     gw2 = GemmDesc{};
     gw2.kind = GK_DW;
-    gw2.a_mn = gw2.b_mn = 1;
+    gw2.a_mn = 1;
     gw2.a = actc.q; gw2.a_rows = rows; gw2.a_cols = I; gw2.sfa = actc.sf; gw2.sfa_bytes = actc.sf_bytes; gw2.sfa_kg = kgt;
-    gw2.b = dygc.q; gw2.b_rows = rows; gw2.b_cols = H; gw2.sfb = dygc.sf; gw2.sfb_bytes = dygc.sf_bytes; gw2.sfb_kg = kgt;
+    gw2.b = dygc.q; gw2.b_rows = H; gw2.b_cols = rp; gw2.sfb = dygc.sf; gw2.sfb_bytes = dygc.sf_bytes; gw2.sfb_kg = kgt;
     gw2.M = I; gw2.N = H;
     gw2.out = dW2; gw2.ld_out = H;
     MOE_TRY(launch_engine(L, s, &st));
     if (st != MOE_OK) return st;
   }
   if (!saved_mx) {
-    MOE_TRY(quant_rows(W13, (int64_t)E * H, 2 * I, w13r, dev_status, s));
+    MOE_TRY(quant_both(W13, (int64_t)E * H, 2 * I, nullptr, &w13r, nullptr, s, nullptr,
+                       DualOut{H, 0, 0, 0}));
     MOE_TRY(quant_cols(x_perm, rows, H, po, E, xpc, dev_status, s));
   }
   {
@@ -473,15 +485,15 @@ moe_status backward_mx(const moe_dims* d, const void* dY, const void* W13, const
     gx.kind = GK_BWD_DX;
     gx.a = dh13r.q; gx.a_rows = rows; gx.a_cols = 2 * I; gx.sfa = dh13r.sf; gx.sfa_bytes = dh13r.sf_bytes; gx.sfa_kg = 2 * I / 128;
     gx.b = w13r.q; gx.b_rows = (int64_t)E * H; gx.b_cols = 2 * I; gx.b_expert_rows = H;
-    gx.sfb = w13r.sf; gx.sfb_bytes = w13r.sf_bytes; gx.sfb_kg = 2 * I / 128;
+    gx.sfb = w13r.sf; gx.sfb_bytes = w13r.sf_bytes; gx.sfb_kg = 2 * I / 128; gx.sfb_seg = mx_tile_slots(H);
     gx.N = H; gx.K = 2 * I;
     gx.out = dxp; gx.ld_out = H;
     GemmDesc& gw = L.prob[1];
     gw = GemmDesc{};
     gw.kind = GK_DW;
-    gw.a_mn = gw.b_mn = 1;
+    gw.a_mn = 1;
     gw.a = xpc.q; gw.a_rows = rows; gw.a_cols = H; gw.sfa = xpc.sf; gw.sfa_bytes = xpc.sf_bytes; gw.sfa_kg = kgt;
-    gw.b = dh13c.q; gw.b_rows = rows; gw.b_cols = 2 * I; gw.sfb = dh13c.sf; gw.sfb_bytes = dh13c.sf_bytes; gw.sfb_kg = kgt;
+    gw.b = dh13c.q; gw.b_rows = 2 * I; gw.b_cols = rp; gw.sfb = dh13c.sf; gw.sfb_bytes = dh13c.sf_bytes; gw.sfb_kg = kgt;
     gw.M = H; gw.N = 2 * I;
     gw.out = dW13; gw.ld_out = 2 * I;
     MOE_TRY(launch_engine(L, s, &st));
@@ -633,6 +645,7 @@ moe_status moe_forward(const moe_dims* d, const void* X, const void* W13, const 
   L.E = d->E;
   L.elem_bytes = es;
   L.padded_offsets = r->padded_offsets;
+  L.counts = r->counts;
   L.max_rows = rows;
   L.status = dev_status;
   L.wait_ns = wait_limit_ns();
@@ -750,6 +763,7 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
   L.elem_bytes = es;
   L.BN = bn;
   L.padded_offsets = r->padded_offsets;
+  L.counts = r->counts;
   L.max_rows = rows;
   L.ready = ready;
   L.ready_target = (debug_flags() & MOE_DEBUG_NEVER_READY) ? 0x7fffffff : d->I / bn;

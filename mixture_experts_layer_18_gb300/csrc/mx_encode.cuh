@@ -34,6 +34,22 @@ __device__ __forceinline__ size_t mma_scale_index(int64_t mn, int kb, int64_t kg
          (size_t)((mn >> 5) & 3) * 4 + (kb & 3);
 }
 
+// Scale slots (MN indices in the atom layout above) of B operands of the
+// block-scaled GEMMs, whose tiles are kMxTileN = 192 B columns wide: each
+// expert segment of `seg` indices is cut into 192-wide tiles and every tile
+// gets two whole atoms (256 slots, the last 64 unused), so the scales of a
+// tile start on an atom boundary and fill the tensor-memory scale columns of
+// its MMAs in order.  Index m of segment e has slot
+// e * mx_tile_slots(seg) + mx_tile_pos(m).
+constexpr int kMxTileN = 192;
+__host__ __device__ __forceinline__ int64_t mx_tile_slots(int64_t seg) {
+  return (seg + kMxTileN - 1) / kMxTileN * 256;
+}
+// slot of index m inside its segment (32-bit, constant divisor)
+__device__ __forceinline__ int mx_tile_pos(int m) {
+  return (m / kMxTileN) * 256 + m % kMxTileN;
+}
+
 // Two E4M3 codes (round to nearest even, saturating), lo in the low byte.
 __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
   return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);

@@ -174,12 +174,21 @@ size_t dual_smem_bytes() {
   return (size_t)2 * kDualTileWords * 4 + 2 * kDualRows * 4;
 }
 
+// Column index of the transposed column-wise output for column c: the
+// block-scaled gate/up GEMM reads W13's encoding with 96 gate and 96 up
+// columns per 192-wide tile (perm 1, C = 2I), the others in order.
+__device__ __forceinline__ int dual_perm(int c, int C, int perm) {
+  if (!perm) return c;
+  const int half = C / 2, tn = kMxTileN / 2;
+  return c < half ? (c / tn) * kMxTileN + c % tn : ((c - half) / tn) * kMxTileN + tn + (c - half) % tn;
+}
+
 template <int SRC>
 __global__ void __launch_bounds__(256, 3) quant_dual_kernel(
     const __nv_bfloat16* __restrict__ src, int R, int C, int ld, const int32_t* __restrict__ rows_dev,
     const int32_t* __restrict__ assign_of_row, int k, int n_assign, const float* __restrict__ gate,
     int32_t* status, uint8_t* __restrict__ qr, uint8_t* __restrict__ sr, uint8_t* __restrict__ qc,
-    uint8_t* __restrict__ sc) {
+    uint8_t* __restrict__ sc, DualOut out) {
   constexpr int TR = kDualRows, PITCH = kDualPitch;
   extern __shared__ __align__(16) uint32_t dsm[];
   uint32_t (*tbuf)[TR][PITCH] = reinterpret_cast<uint32_t (*)[TR][PITCH]>(dsm);   // [2]
@@ -259,6 +268,13 @@ __global__ void __launch_bounds__(256, 3) quant_dual_kernel(
     cp_async_wait_prev();
     __syncthreads();   // tile t in buffer b, from every thread's copies
     const uint32_t (*tile)[PITCH] = tbuf[b];
+    // B-operand outputs: the tile's rows lie in one segment (segment lengths
+    // are multiples of 128), so its segment index is computed once
+    const int64_t rseg = out.row_seg > 0 ? r0 / out.row_seg : 0;
+    const int64_t rslot0 = out.row_seg > 0 ? rseg * mx_tile_slots(out.row_seg) : 0;
+    const int rbase = out.row_seg > 0 ? (int)(r0 - rseg * out.row_seg) : 0;
+    const int64_t cseg = out.col_ld > 0 ? r0 / out.col_seg : 0;
+    const int ckr0 = out.col_ld > 0 ? (int)(r0 - cseg * out.col_seg) : 0;
     if (threadIdx.x < 128) {
       // column-wise: thread = (32-row block, column pair); the 32 words of
       // its two columns in registers, maxima and codes from them
@@ -278,6 +294,34 @@ __global__ void __launch_bounds__(256, 3) quant_dual_kernel(
         }
         const int sb0 = mx_scale_byte(absmax_lo(acc)), sb1 = mx_scale_byte(absmax_hi(acc));
         const float inv0 = mx_inv_scale(sb0), inv1 = mx_inv_scale(sb1);
+        if (out.col_ld > 0) {
+          // transposed (K-major B): each column's 32 codes are 32 contiguous
+          // bytes of its output row; scales in the 192-column tile slots
+          const int kr = ckr0 + 32 * rb;
+          const int64_t kg = (out.col_seg + 127) / 128;
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t o[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t wa = h2 ? (w[4 * i] >> 16) | (w[4 * i + 1] & 0xFFFF0000u)
+                                     : (w[4 * i] & 0xFFFFu) | (w[4 * i + 1] << 16);
+              const uint32_t wb = h2 ? (w[4 * i + 2] >> 16) | (w[4 * i + 3] & 0xFFFF0000u)
+                                     : (w[4 * i + 2] & 0xFFFFu) | (w[4 * i + 3] << 16);
+              const float iv = h2 ? inv1 : inv0;
+              o[i] = (uint32_t)e4m3x2(bf16_lo(wa) * iv, bf16_hi(wa) * iv) |
+                     ((uint32_t)e4m3x2(bf16_lo(wb) * iv, bf16_hi(wb) * iv) << 16);
+            }
+            const int pc = dual_perm(c0 + 2 * j + h2, C, out.col_perm);
+            const int64_t orow = cseg * C + pc;
+            uint4* d = reinterpret_cast<uint4*>(qc + (size_t)orow * out.col_ld + kr);
+            d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            const int64_t slot = cseg * mx_tile_slots(C) + mx_tile_pos(pc);
+            sc[mma_scale_index(slot, kr >> 5, kg)] = (uint8_t)(h2 ? sb1 : sb0);
+          }
+          continue;
+        }
         uint16_t* d = reinterpret_cast<uint16_t*>(qc + (size_t)(r0 + 32 * rb) * C + c0 + 2 * j);
 #pragma unroll
         for (int r = 0; r < 32; ++r)
@@ -288,7 +332,7 @@ __global__ void __launch_bounds__(256, 3) quant_dual_kernel(
     } else {
       // row-wise: thread = (row, 32-column block), tile rows x 4 tasks over
       // threads 128-255
-      for (int task = threadIdx.x - 128; task < 32 * nrb * 4; task += 128) {
+      for (int task = threadIdx.x - 128; qr && task < 32 * nrb * 4; task += 128) {
         const int er = task >> 2, bb = task & 3;
         uint32_t w[16];
         uint32_t acc = 0;
@@ -311,7 +355,8 @@ __global__ void __launch_bounds__(256, 3) quant_dual_kernel(
         uint4* d = reinterpret_cast<uint4*>(qr + (size_t)(r0 + er) * C + c0 + 32 * bb);
         d[0] = make_uint4(o[0], o[1], o[2], o[3]);
         d[1] = make_uint4(o[4], o[5], o[6], o[7]);
-        sr[mma_scale_index(r0 + er, (c0 >> 5) + bb, nct)] = (uint8_t)sbv;
+        const int64_t mn = out.row_seg > 0 ? rslot0 + mx_tile_pos(rbase + er) : r0 + er;
+        sr[mma_scale_index(mn, (c0 >> 5) + bb, nct)] = (uint8_t)sbv;
       }
     }
     __syncthreads();   // buffer b and its gates are free for the next tiles
@@ -354,7 +399,11 @@ cudaError_t launch_quantize(const void* src, int R, int C, int ld, int axis,
 
 cudaError_t launch_quantize_dual(const void* src, int R, int C, int ld, const int32_t* rows_dev,
                                  uint8_t* qr, uint8_t* sr, uint8_t* qc, uint8_t* sc,
-                                 cudaStream_t s, const DualGather* gather) {
+                                 cudaStream_t s, const DualGather* gather, const DualOut* outp) {
+  const DualOut out = outp ? *outp : DualOut{};
+  if (out.col_ld > 0 && (out.col_seg <= 0 || out.col_seg % 128 || out.col_ld % 16 ||
+                         (out.col_perm && (C / 2) % (kMxTileN / 2))))
+    return cudaErrorInvalidValue;
   const int64_t tiles = (int64_t)((R + kDualRows - 1) / kDualRows) * (C / 128);
   if (tiles == 0) return cudaSuccess;
   const __nv_bfloat16* x = (const __nv_bfloat16*)src;
@@ -384,19 +433,19 @@ cudaError_t launch_quantize_dual(const void* src, int R, int C, int ld, const in
     const size_t sm = dual_smem_bytes<0>();
     if (!setup(quant_dual_kernel<0>, sm, 0)) return cudaErrorInvalidValue;
     quant_dual_kernel<0><<<blocks, 256, sm, s>>>(x, R, C, ld, rows_dev, nullptr, 1, 0, nullptr,
-                                                 nullptr, qr, sr, qc, sc);
+                                                 nullptr, qr, sr, qc, sc, out);
   } else if (!gather->gate) {
     const size_t sm = dual_smem_bytes<1>();
     if (!setup(quant_dual_kernel<1>, sm, 1)) return cudaErrorInvalidValue;
     quant_dual_kernel<1><<<blocks, 256, sm, s>>>(x, R, C, ld, rows_dev, gather->assign_of_row,
                                                  gather->k, gather->n_assign, nullptr,
-                                                 gather->status, qr, sr, qc, sc);
+                                                 gather->status, qr, sr, qc, sc, out);
   } else {
     const size_t sm = dual_smem_bytes<2>();
     if (!setup(quant_dual_kernel<2>, sm, 2)) return cudaErrorInvalidValue;
     quant_dual_kernel<2><<<blocks, 256, sm, s>>>(x, R, C, ld, rows_dev, gather->assign_of_row,
                                                  gather->k, gather->n_assign, gather->gate,
-                                                 gather->status, qr, sr, qc, sc);
+                                                 gather->status, qr, sr, qc, sc, out);
   }
   return cudaGetLastError();
 }

@@ -58,3 +58,12 @@ def atom_byte(mn, kb, kgroups):
     mn = np.asarray(mn)
     kb = np.asarray(kb)
     return ((mn // 128) * kgroups + kb // 4) * 512 + (mn % 32) * 16 + ((mn // 32) % 4) * 4 + kb % 4
+
+
+def tile_slot(mn, seg):
+    """Scale slot of B-operand index mn of the block-scaled GEMMs, as declared
+    in moe.h: each segment of `seg` indices is cut into 192-wide tiles and
+    each tile owns 256 slots (two atoms)."""
+    mn = np.asarray(mn)
+    e, m = mn // seg, mn % seg
+    return e * (-(-seg // 192) * 256) + (m // 192) * 256 + m % 192

@@ -111,6 +111,6 @@ def test_null_and_misaligned_pointers_rejected_on_host():
 
 
 def test_status_strings():
-    for code in range(6):
+    for code in range(7):
         assert M.moe_status_string(code)
     assert M.moe_status_string(42) == "unknown status"

@@ -8,7 +8,7 @@ import pytest
 from oracle import moe_oracle as O
 from workloads import CONFIGS, MoEConfig, make_inputs
 
-from _common import TOL_BF16, TOL_MXFP8, F32View, atom_byte, rel_err, to_device, to_f64
+from _common import TOL_BF16, TOL_MXFP8, F32View, atom_byte, rel_err, tile_slot, to_device, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -31,9 +31,12 @@ def _oracle_inputs(inp):
     return {k: (F32View(v) if k != "logits" else v) for k, v in inp.items()}
 
 
-SMALL = [MoEConfig("mx_a", 512, 256, 8, 2, 256, "bf16"),
-         MoEConfig("mx_b", 700, 512, 16, 4, 256, "bf16"),
-         MoEConfig("mx_skew", 600, 256, 32, 4, 256, "bf16", skew=True)]
+# The block-scaled GEMMs run 192-column tiles over K stages of 128: I is a
+# multiple of 384, and H = 256 / 512 leaves a ragged last tile on the H-wide
+# outputs.
+SMALL = [MoEConfig("mx_a", 512, 256, 8, 2, 384, "bf16"),
+         MoEConfig("mx_b", 700, 512, 16, 4, 384, "bf16"),
+         MoEConfig("mx_skew", 600, 256, 32, 4, 384, "bf16", skew=True)]
 
 
 @pytest.mark.parametrize("mode", ["mxfp8", "fp8_bwd"])
@@ -133,12 +136,13 @@ def test_saved_encodings_bit_exact():
     assert np.array_equal(q, cq)
     rb, c = np.meshgrid(np.arange(tpad // 32), np.arange(H), indexing="ij")
     assert np.array_equal(sv[lay.x_col_sf + atom_byte(c, rb, rp // 128)], cs)
-    for name, W, R, C in (("w13_row", inp["W13"], E * H, 2 * I), ("w2_row", inp["W2"], E * I, H)):
+    for name, W, R, C, seg in (("w13_row", inp["W13"], E * H, 2 * I, H),
+                               ("w2_row", inp["W2"], E * I, H, I)):
         rq, rs = O.quantize_mxfp8(bf16_bits_to_f32(W).reshape(R, C).astype(np.float64), 1)
         off_q, off_s = getattr(lay, name + "_q"), getattr(lay, name + "_sf")
         assert np.array_equal(sv[off_q: off_q + R * C].reshape(R, C), rq), name
         r, kb = np.meshgrid(np.arange(R), np.arange(C // 32), indexing="ij")
-        assert np.array_equal(sv[off_s + atom_byte(r, kb, C // 128)], rs), name
+        assert np.array_equal(sv[off_s + atom_byte(tile_slot(r, seg), kb, C // 128)], rs), name
 
 
 def test_activation_encodings_from_the_epilogue():
