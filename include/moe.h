@@ -231,10 +231,10 @@ moe_status moe_forward(const moe_dims* dims, const void* X, const void* W13,
  *   dX[t]  = sum_j (dh13 W13_e^T)[row_of_assign[t*k + j]],
  *   dW13_e = X_perm_e^T dh13_e,  dW2_e = A_e^T (gate * dY)_perm_e,
  * experts with no token get zero weight gradients.  The activation-gradient
- * GEMMs and the weight-gradient GEMMs run as co-scheduled tiles of one
- * persistent launch.  In MOE_BF16 mode dW2_e = (gate * A)_e^T dY_perm_e (the
- * same product, from the gated `act` the forward saved: no gated copy of dY
- * is made).
+ * GEMMs and the weight-gradient GEMMs run as co-scheduled tiles of
+ * persistent launches ({D + dSwiGLU, dW2}, then {dX, dW13}).  In MOE_BF16
+ * mode dW2_e = (gate * A)_e^T dY_perm_e (the same product, from the gated
+ * `act` the forward saved: no gated copy of dY is made).
  *   dY [T, H]; dX [T, H]; dW13 [E, H, 2I]; dW2 [E, I, H]; dgate float [T, k]
  *   saved  the buffer written by moe_forward with save_for_backward = 1.
  *   ws     MOE_WS_BACKWARD workspace. */
@@ -287,15 +287,20 @@ moe_status moe_quantize_mxfp8_dual(const void* src, int R, int C, int ld,
 const char* moe_status_string(moe_status s);
 
 /* Test and diagnosis hooks.  `wait_limit_ns` bounds every device-side wait
- * (0 restores the default of one second).  Flag MOE_DEBUG_NEVER_READY makes
- * the co-scheduled backward wait on a readiness counter that is never
- * bumped, so the bounded wait runs out and MOE_ERR_TIMEOUT is reported.
- * Flag MOE_DEBUG_SINGLE_CTA runs the bf16 GEMMs with single-CTA 128-row
- * tiles instead of 256-row tiles over an SM pair (for A/B comparison).
- * Flag MOE_DEBUG_SPLIT_BACKWARD runs the four bf16 gradient GEMMs as four
- * consecutive launches instead of one co-scheduled launch (to time each).
+ * (0 restores the default of one second).  The bf16 backward runs its four
+ * gradient GEMMs as two co-scheduled persistent launches, {D + dSwiGLU, dW2}
+ * then {dX, dW13} (no tile waits on another CTA).  Flag
+ * MOE_DEBUG_ONE_LAUNCH_BACKWARD runs all four in one persistent cooperative
+ * launch instead, where dX / dW13 tiles wait (bounded) on readiness
+ * counters bumped by the D tiles; MOE_DEBUG_NEVER_READY (implies it) makes
+ * them wait on a counter that is never bumped, so the bounded wait runs out
+ * and MOE_ERR_TIMEOUT is reported.  Flag MOE_DEBUG_SINGLE_CTA runs the bf16
+ * and MXFP8 GEMMs with single-CTA 128-row tiles instead of 256-row tiles
+ * over an SM pair (for A/B comparison).  Flag MOE_DEBUG_SPLIT_BACKWARD runs
+ * the four bf16 gradient GEMMs as four consecutive launches (to time each).
  * Process-wide; not thread-safe against concurrent calls. */
-enum { MOE_DEBUG_NEVER_READY = 1, MOE_DEBUG_SINGLE_CTA = 2, MOE_DEBUG_SPLIT_BACKWARD = 4 };
+enum { MOE_DEBUG_NEVER_READY = 1, MOE_DEBUG_SINGLE_CTA = 2, MOE_DEBUG_SPLIT_BACKWARD = 4,
+       MOE_DEBUG_ONE_LAUNCH_BACKWARD = 8 };
 void moe_set_debug(int flags, int64_t wait_limit_ns);
 
 /* Diagnosis hook: a bounded side load.  Launches `ctas` thread blocks on

@@ -17,7 +17,7 @@ __all__ = [
     "MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_CUDA",
     "MOE_ERR_TIMEOUT", "MOE_ERR_BAD_INDEX", "MOE_ERR_BAD_INPUT", "MOE_F32", "MOE_BF16", "MOE_MXFP8",
     "MOE_FP8_BWD", "MOE_WS_ROUTE", "MOE_WS_FORWARD", "MOE_WS_BACKWARD",
-    "MOE_DEBUG_NEVER_READY", "MOE_DEBUG_SINGLE_CTA", "MOE_DEBUG_SPLIT_BACKWARD", "moe_dims", "moe_route_out", "moe_saved_layout",
+    "MOE_DEBUG_NEVER_READY", "MOE_DEBUG_SINGLE_CTA", "MOE_DEBUG_SPLIT_BACKWARD", "MOE_DEBUG_ONE_LAUNCH_BACKWARD", "moe_dims", "moe_route_out", "moe_saved_layout",
     "lib", "header_functions", "moe_max_rows", "moe_workspace_size",
     "moe_saved_layout_of", "moe_route", "moe_route_noalloc", "moe_route_backward", "moe_forward", "moe_backward",
     "moe_quantize_mxfp8", "moe_quantize_mxfp8_dual", "moe_status_string", "moe_set_debug", "moe_set_gemm_events", "moe_debug_occupy",
@@ -31,6 +31,7 @@ MOE_WS_ROUTE, MOE_WS_FORWARD, MOE_WS_BACKWARD = 0, 1, 2
 MOE_DEBUG_NEVER_READY = 1
 MOE_DEBUG_SINGLE_CTA = 2
 MOE_DEBUG_SPLIT_BACKWARD = 4
+MOE_DEBUG_ONE_LAUNCH_BACKWARD = 8
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                       "include", "moe.h")

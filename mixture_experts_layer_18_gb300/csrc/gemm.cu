@@ -143,8 +143,9 @@ struct Cfg {
   // takes to issue a stage's three scale copies, four MMAs and commit, or
   // its five TMA loads: the issue work is split over two more warps, one
   // loading B and its scales, one copying the scales into tensor memory.
-  static constexpr bool SPLIT_ISSUE = MX;
-  static constexpr int EXTRA_WARPS = SPLIT_ISSUE ? 2 : 0;
+  static constexpr bool SPLIT_LOAD = MX;
+  static constexpr bool SPLIT_ISSUE = MX;          // scale-copier warp
+  static constexpr int EXTRA_WARPS = (SPLIT_LOAD ? 1 : 0) + (SPLIT_ISSUE ? 1 : 0);
   static constexpr int THREADS = 64 + 32 * EPI_WARPS * EPI_GROUPS + 32 * EXTRA_WARPS;
   static constexpr int STG_BYTES = EPI_WARPS * EPI_GROUPS * 4096;   // staging (2 x 2 KB per warp)
   static constexpr int FIXED_BYTES = STG_BYTES + 1024 /*align*/ + 512 /*bars*/ +
@@ -1085,7 +1086,7 @@ __global__ void __launch_bounds__(Cfg<In, BN, PAIR>::THREADS, 1)
   if (warp == 0) {
     if ((threadIdx.x & 31) == 0)
       producer_role<C>(P, cum, total, s_po, s_pt, rank, stages, sfreg, full, empty, wc,
-                       C::SPLIT_ISSUE ? 0 : -1);
+                       C::SPLIT_LOAD ? 0 : -1);
     __syncwarp();
   } else if (warp == 1) {
     if ((threadIdx.x & 31) == 0 && rank == 0)
@@ -1094,11 +1095,11 @@ __global__ void __launch_bounds__(Cfg<In, BN, PAIR>::THREADS, 1)
     __syncwarp();
   } else if (warp < EPI_END) {
     epilogue_role<C, Out>(P, cum, total, s_po, s_pt, rank, tfull, tempty, tmem_base, s_go, stg, wc);
-  } else if (warp == EPI_END) {
+  } else if (C::SPLIT_LOAD && warp == EPI_END) {
     if ((threadIdx.x & 31) == 0)
       producer_role<C>(P, cum, total, s_po, s_pt, rank, stages, sfreg, full, empty, wc, 1);
     __syncwarp();
-  } else {
+  } else if constexpr (C::SPLIT_ISSUE) {
     if ((threadIdx.x & 31) == 0 && rank == 0)
       sf_role<C>(P, cum, total, s_po, s_pt, sfreg, full, sfready, drain2, tmem_base, wc);
     __syncwarp();

@@ -749,7 +749,10 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
     MOE_TRY(launch_gather_grad(dY, dy_perm, dyg_perm, d->H, es, d->top_k, n_assign,
                                r->assign_of_row, r->gate, r->padded_offsets, d->E, rows,
                                dev_status, s));
-  MOE_TRY(cudaMemsetAsync(ready, 0, ((rows + 127) / 128 + 1) * sizeof(int32_t), s));
+  // one co-scheduled launch with readiness counters (diagnosis flags only)
+  const bool one_launch = d->mode != MOE_F32 &&
+                          (debug_flags() & (MOE_DEBUG_ONE_LAUNCH_BACKWARD | MOE_DEBUG_NEVER_READY));
+  if (one_launch) MOE_TRY(cudaMemsetAsync(ready, 0, ((rows + 127) / 128 + 1) * sizeof(int32_t), s));
   const bool f32 = d->mode == MOE_F32;
   const int64_t lt = ld_t(d);
   float* act_t = reinterpret_cast<float*>(wb + w.act_t);
@@ -770,10 +773,9 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
   L.status = dev_status;
   L.wait_ns = wait_limit_ns();
 
-  // D = dY_perm W2^T with the dSwiGLU / d(gate) epilogue (bumps readiness)
+  // D = dY_perm W2^T with the dSwiGLU / d(gate) epilogue
   GemmDesc gd{};
   gd.kind = GK_BWD_D;
-  gd.signal = 1;
   gd.a = dy_perm; gd.a_rows = rows; gd.a_cols = d->H;
   gd.b = W2; gd.b_rows = (int64_t)d->E * d->I; gd.b_cols = d->H;
   gd.N = d->I; gd.K = d->H; gd.b_expert_rows = d->I; gd.I = d->I;
@@ -787,14 +789,14 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
   gw2.kind = GK_DW;
   gw2.M = d->I; gw2.N = d->H;
   gw2.out = dW2; gw2.ld_out = d->H;
-  // dXp = dh13 W13^T   (waits for the m-block's D tiles)
+  // dXp = dh13 W13^T
   GemmDesc gx{};
   gx.kind = GK_BWD_DX;
   gx.a = dh13; gx.a_rows = rows; gx.a_cols = 2 * d->I;
   gx.b = W13; gx.b_rows = (int64_t)d->E * d->H; gx.b_cols = 2 * d->I;
   gx.N = d->H; gx.K = 2 * d->I; gx.b_expert_rows = d->H;
   gx.out = dxp; gx.ld_out = d->H;
-  // dW13_e = X_perm_e^T dh13_e   (waits for all D tiles of expert e)
+  // dW13_e = X_perm_e^T dh13_e
   GemmDesc gw13{};
   gw13.kind = GK_DW;
   gw13.M = d->H; gw13.N = 2 * d->I;
@@ -807,15 +809,11 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
     gw2.a = act; gw2.a_rows = rows; gw2.a_cols = d->I;
     // dW2 = (gate * A)^T dY_perm (bf16: `act` holds gate * A)
     gw2.b = gate_on_act(d) ? dy_perm : dyg_perm; gw2.b_rows = rows; gw2.b_cols = d->H;
-    gx.dep = DEP_MBLOCK;
-    gw13.dep = DEP_EXPERT;
     gw13.a_mn = gw13.b_mn = 1;
     gw13.a = x_perm; gw13.a_rows = rows; gw13.a_cols = d->H;
     gw13.b = dh13; gw13.b_rows = rows; gw13.b_cols = 2 * d->I;
     if (debug_flags() & MOE_DEBUG_SPLIT_BACKWARD) {
       // one launch per gradient GEMM, in dependency order (diagnosis only)
-      gd.signal = 0;
-      gx.dep = gw13.dep = DEP_NONE;
       const GemmDesc parts[4] = {gd, gw2, gx, gw13};
       L.nprob = 1;
       for (const GemmDesc& gp : parts) {
@@ -823,12 +821,33 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
         MOE_TRY(launch_engine(L, s, &st));
         if (st != MOE_OK) return st;
       }
-    } else {
+    } else if (one_launch) {
+      // all four in one persistent launch: D tiles publish their m-block,
+      // dX tiles wait for their m-block, dW13 tiles for their expert's
+      // m-blocks (bounded waits; a cooperative launch, see gemm.cu)
+      gd.signal = 1;
+      gx.dep = DEP_MBLOCK;
+      gw13.dep = DEP_EXPERT;
       L.nprob = 4;
       L.prob[0] = gd;
       L.prob[1] = gw2;
       L.prob[2] = gx;
       L.prob[3] = gw13;
+      MOE_TRY(launch_engine(L, s, &st));
+      if (st != MOE_OK) return st;
+    } else {
+      // Co-scheduled in two persistent launches ([OB] "Overlapping Backward
+      // Pass": the activation-gradient GEMMs need the weights, not the
+      // weight gradients): {D + dSwiGLU, dW2}, then {dX, dW13}, the only
+      // dependency (dh13, written by D, read by dX and dW13) ordered by the
+      // stream, so no tile waits on another CTA.
+      L.nprob = 2;
+      L.prob[0] = gd;
+      L.prob[1] = gw2;
+      MOE_TRY(launch_engine(L, s, &st));
+      if (st != MOE_OK) return st;
+      L.prob[0] = gx;
+      L.prob[1] = gw13;
       MOE_TRY(launch_engine(L, s, &st));
       if (st != MOE_OK) return st;
     }

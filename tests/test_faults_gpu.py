@@ -105,13 +105,16 @@ def test_invalid_arguments_rejected_before_launch():
     assert L.device_status() == 0
 
 
-def test_backward_while_half_the_gpu_is_busy():
+@pytest.mark.parametrize("flags", [0, M.MOE_DEBUG_ONE_LAUNCH_BACKWARD])
+def test_backward_while_half_the_gpu_is_busy(flags):
     """A bounded side kernel on another stream holds about half of the SMs
     (one block with 200 KB of shared memory per SM, 76 blocks, 300 ms) while
-    a whole step runs with a 20 ms device wait limit.  The co-scheduled
-    backward's tiles wait on tiles of other CTAs, so its launch must not
-    start on the SMs that happen to be free and then wait for CTAs that
-    cannot be placed: the step finishes with status 0 and oracle parity."""
+    a whole step runs with a 20 ms device wait limit: status 0 and oracle
+    parity, both for the default backward (two co-scheduled launches, no
+    tile waits on another CTA) and for the one-launch form, whose dX / dW13
+    tiles wait on D tiles of other CTAs, so its launch must not start on the
+    SMs that happen to be free and then wait for CTAs that cannot be placed
+    (a cooperative launch)."""
     import torch
     from mixture_experts_layer_18_gb300.layer import MoELayer
     cfg = MoEConfig("busy", 4096, 1024, 16, 4, 512, "bf16")
@@ -124,7 +127,7 @@ def test_backward_while_half_the_gpu_is_busy():
     assert L.device_status() == 0
     side = torch.cuda.Stream()
     try:
-        M.moe_set_debug(0, 20_000_000)
+        M.moe_set_debug(flags, 20_000_000)
         L.clear_status()
         torch.cuda.synchronize()
         assert M.moe_debug_occupy(76, 200 * 1024, 300_000_000, side.cuda_stream) == M.MOE_OK
@@ -151,3 +154,23 @@ def test_occupy_hook_rejects_unbounded_requests():
     assert M.moe_debug_occupy(0, 0, 1000, None) == M.MOE_ERR_INVALID_ARG
     assert M.moe_debug_occupy(4, 300 * 1024, 1000, None) == M.MOE_ERR_INVALID_ARG
     assert M.moe_debug_occupy(4, 1024, 2_000_000_000, None) == M.MOE_ERR_INVALID_ARG
+
+
+def test_one_launch_backward_matches_two_launches():
+    """The one-launch co-scheduled backward (readiness counters) and the
+    default two launches run the same tiles on the same operands: identical
+    results bit for bit."""
+    import torch
+    inp, L, io, dev = _setup()
+    _step(L, io, dev)
+    torch.cuda.synchronize()
+    a = {k: v.clone() for k, v in io.items()}
+    try:
+        M.moe_set_debug(M.MOE_DEBUG_ONE_LAUNCH_BACKWARD, 0)
+        _step(L, io, dev)
+        torch.cuda.synchronize()
+    finally:
+        M.moe_set_debug(0, 0)
+    assert L.device_status() == 0
+    for k in a:
+        assert torch.equal(a[k], io[k]), k
