@@ -139,11 +139,13 @@ struct Cfg {
   // has two tiles' worth of MMA time for its epilogue).
   static constexpr int EPI_WARPS = 4;             // warps per group
   static constexpr int EPI_GROUPS = MX ? 2 : 1;
-  // Block-scaled stages hold 384 tensor cycles of MMAs, less than one thread
-  // takes to issue a stage's three scale copies, four MMAs and commit, or
-  // its five TMA loads: the issue work is split over two more warps, one
-  // loading B and its scales, one copying the scales into tensor memory.
-  static constexpr bool SPLIT_LOAD = MX;
+  // Issue work: one thread issuing a stage's TMA loads (and, block-scaled,
+  // the three scale copies beside the four MMAs) takes about as long as the
+  // stage's MMAs run (384 tensor cycles for block-scaled stages, 512 for
+  // bf16), so on SM pairs a second producer warp loads B (and its scales)
+  // while warp 0 loads A, and block-scaled runs add a warp that copies the
+  // scales into tensor memory.
+  static constexpr bool SPLIT_LOAD = PAIR == 2;
   static constexpr bool SPLIT_ISSUE = MX;          // scale-copier warp
   static constexpr int EXTRA_WARPS = (SPLIT_LOAD ? 1 : 0) + (SPLIT_ISSUE ? 1 : 0);
   static constexpr int THREADS = 64 + 32 * EPI_WARPS * EPI_GROUPS + 32 * EXTRA_WARPS;
