@@ -72,11 +72,10 @@ cudaError_t current_context_id(unsigned long long* id) {
 
 namespace {
 
-// Holds its CTA (and the CTA's shared memory) for `ns` nanoseconds, then
-// returns: the bounded side load of moe_debug_occupy.
+// Holds its CTA (and the dynamic shared memory it was launched with, which
+// it never touches) for `ns` nanoseconds, then returns: the bounded side
+// load of moe_debug_occupy.
 __global__ void occupy_kernel(uint64_t ns) {
-  extern __shared__ uint8_t hold[];
-  if (threadIdx.x == 0) reinterpret_cast<volatile uint8_t*>(hold)[0] = 1;
   const uint64_t t0 = global_ns();
   while (global_ns() - t0 < ns) __nanosleep(2000);
 }

@@ -275,7 +275,40 @@ __global__ void __launch_bounds__(256, 3) quant_dual_kernel(
     const int rbase = out.row_seg > 0 ? (int)(r0 - rseg * out.row_seg) : 0;
     const int64_t cseg = out.col_ld > 0 ? r0 / out.col_seg : 0;
     const int ckr0 = out.col_ld > 0 ? (int)(r0 - cseg * out.col_seg) : 0;
-    if (threadIdx.x < 128) {
+    if (threadIdx.x < 128 && qc && out.col_ld > 0) {
+      // column-wise, stored transposed (K-major B): thread = one column of
+      // the tile, whose codes for the tile's 32-row blocks are consecutive
+      // bytes of its output row, written as whole 32-byte pieces in turn
+      const int c = threadIdx.x, j = c >> 1, hi = c & 1;
+      const int pc = dual_perm(c0 + c, C, out.col_perm);
+      const int64_t orow = cseg * C + pc;
+      const int64_t kg = (out.col_seg + 127) / 128;
+      const int64_t slot = cseg * mx_tile_slots(C) + mx_tile_pos(pc);
+      uint4* dst = reinterpret_cast<uint4*>(qc + (size_t)orow * out.col_ld + ckr0);
+      for (int rb = 0; rb < nrb; ++rb) {
+        float v[32];
+        float am = 0.f;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+          const uint32_t wv = tile[32 * rb + r][j];
+          float x = hi ? bf16_hi(wv) : bf16_lo(wv);
+          if constexpr (SRC == 2)   // gate-scaled rows, rounded to bf16 once
+            x = __bfloat162float(__float2bfloat16_rn(s_g[b * TR + 32 * rb + r] * x));
+          v[r] = x;
+          am = fmaxf(am, fabsf(x));
+        }
+        const int sbc = mx_scale_byte(am);
+        const float inv = mx_inv_scale(sbc);
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          o[i] = (uint32_t)e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv) |
+                 ((uint32_t)e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv) << 16);
+        dst[2 * rb] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[2 * rb + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+        sc[mma_scale_index(slot, (ckr0 >> 5) + rb, kg)] = (uint8_t)sbc;
+      }
+    } else if (threadIdx.x < 128) {
       // column-wise: thread = (32-row block, column pair); the 32 words of
       // its two columns in registers, maxima and codes from them
       for (int rb = threadIdx.x >> 6; rb < nrb; rb += 2) {
@@ -294,34 +327,6 @@ __global__ void __launch_bounds__(256, 3) quant_dual_kernel(
         }
         const int sb0 = mx_scale_byte(absmax_lo(acc)), sb1 = mx_scale_byte(absmax_hi(acc));
         const float inv0 = mx_inv_scale(sb0), inv1 = mx_inv_scale(sb1);
-        if (out.col_ld > 0) {
-          // transposed (K-major B): each column's 32 codes are 32 contiguous
-          // bytes of its output row; scales in the 192-column tile slots
-          const int kr = ckr0 + 32 * rb;
-          const int64_t kg = (out.col_seg + 127) / 128;
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            uint32_t o[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint32_t wa = h2 ? (w[4 * i] >> 16) | (w[4 * i + 1] & 0xFFFF0000u)
-                                     : (w[4 * i] & 0xFFFFu) | (w[4 * i + 1] << 16);
-              const uint32_t wb = h2 ? (w[4 * i + 2] >> 16) | (w[4 * i + 3] & 0xFFFF0000u)
-                                     : (w[4 * i + 2] & 0xFFFFu) | (w[4 * i + 3] << 16);
-              const float iv = h2 ? inv1 : inv0;
-              o[i] = (uint32_t)e4m3x2(bf16_lo(wa) * iv, bf16_hi(wa) * iv) |
-                     ((uint32_t)e4m3x2(bf16_lo(wb) * iv, bf16_hi(wb) * iv) << 16);
-            }
-            const int pc = dual_perm(c0 + 2 * j + h2, C, out.col_perm);
-            const int64_t orow = cseg * C + pc;
-            uint4* d = reinterpret_cast<uint4*>(qc + (size_t)orow * out.col_ld + kr);
-            d[0] = make_uint4(o[0], o[1], o[2], o[3]);
-            d[1] = make_uint4(o[4], o[5], o[6], o[7]);
-            const int64_t slot = cseg * mx_tile_slots(C) + mx_tile_pos(pc);
-            sc[mma_scale_index(slot, kr >> 5, kg)] = (uint8_t)(h2 ? sb1 : sb0);
-          }
-          continue;
-        }
         uint16_t* d = reinterpret_cast<uint16_t*>(qc + (size_t)(r0 + 32 * rb) * C + c0 + 2 * j);
 #pragma unroll
         for (int r = 0; r < 32; ++r)
