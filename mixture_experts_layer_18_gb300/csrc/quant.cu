@@ -139,7 +139,10 @@ __global__ void __launch_bounds__(256) quant_colwise_kernel(const __nv_bfloat16*
 // stores).  Codes and scale bytes are those of the two kernels above.
 // Rows at or past `rows` (a device value, e.g. the padded row total) are
 // neither read nor written; they start on a 32-row boundary.  qc == nullptr
-// skips the column-wise output.
+// skips the column-wise output.  Gathered passes copy each tile's row
+// assignments into shared memory two tiles ahead of its data copies, and
+// its gates beside its data, all with asynchronous copies, so no thread ever
+// waits on a global index load before issuing a tile's copies.
 // SRC: 0 = row r of src; 1 = token row assign_of_row[r] / k of src (the
 // dispatch gather; pad rows read as 0); 2 = the same gather, with the
 // column-wise encoding taken of gate[a] * row rounded to bf16 (the
@@ -154,6 +157,13 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* src, int 
                "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
                : "memory");
 }
+// 4-byte asynchronous copy global -> shared; src_bytes 0 writes zeros.
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(smem_dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_prev() {   // all but the newest group landed
   asm volatile("cp.async.wait_group 1;" ::: "memory");
@@ -169,9 +179,10 @@ __device__ __forceinline__ uint32_t absmax2(uint32_t acc, uint32_t w) {
 __device__ __forceinline__ float absmax_lo(uint32_t acc) { return __uint_as_float(acc << 16); }
 __device__ __forceinline__ float absmax_hi(uint32_t acc) { return __uint_as_float(acc & 0xFFFF0000u); }
 
+// two tile buffers, then gates [2][rows] and row assignments [3][rows]
 template <int SRC>
 size_t dual_smem_bytes() {
-  return (size_t)2 * kDualTileWords * 4 + 2 * kDualRows * 4;
+  return (size_t)2 * kDualTileWords * 4 + 5 * kDualRows * 4;
 }
 
 // Column index of the transposed column-wise output for column c: the
@@ -193,39 +204,25 @@ __global__ void __launch_bounds__(256, 3) quant_dual_kernel(
   extern __shared__ __align__(16) uint32_t dsm[];
   uint32_t (*tbuf)[TR][PITCH] = reinterpret_cast<uint32_t (*)[TR][PITCH]>(dsm);   // [2]
   float* s_g = reinterpret_cast<float*>(dsm + 2 * kDualTileWords);   // [2][TR] gates (SRC 2)
+  int32_t* s_a = reinterpret_cast<int32_t*>(s_g + 2 * TR);            // [3][TR] assignments
   const int rows = rows_dev ? min(*rows_dev, R) : R;
   const int nct = C / 128, nrt = (rows + TR - 1) / TR;
   const int64_t ntiles = (int64_t)nrt * nct;
   const int64_t kg_rows = (R + 127) / 128;
-  // Gathered tiles: the assignment (and gate) of each of this thread's rows
-  // is loaded one tile ahead of its copies, so issuing a tile's copies never
-  // waits on the index load.
-  constexpr int NCH = TR / 16;                     // 16-byte chunks per thread per tile
-  int ai[NCH];
-  float gi[NCH];
-  auto load_rows = [&](int64_t t) {
-    const int rt = (int)(t / nct);
-#pragma unroll
-    for (int i = 0; i < NCH; ++i) {
-      const int r = rt * TR + ((threadIdx.x + 256 * i) >> 4);
-      ai[i] = -1;
-      gi[i] = 0.f;
-      if constexpr (SRC != 0) {
-        if (r < rows) {
-          const int a = assign_of_row[r];
-          const int c = (threadIdx.x + 256 * i) & 15;
-          if (a >= n_assign && c == 0) report(status, MOE_ERR_BAD_INDEX);
-          if (a >= 0 && a < n_assign) {
-            ai[i] = a;
-            if constexpr (SRC == 2) gi[i] = gate[a];
-          }
-        }
-      }
+  // Gathered tiles: the assignment of each row of tile t lands in slot
+  // (t's iteration) % 3 two tiles before the tile's data copies are issued
+  // (rows at or past `rows` read as 0 and are skipped by the row test).
+  auto copy_rows = [&](int64_t t, int slot) {
+    if (SRC != 0 && threadIdx.x < TR) {
+      const int r = (int)(t / nct) * TR + threadIdx.x;
+      const bool in = r < rows;
+      cp_async4(&s_a[slot * TR + threadIdx.x], assign_of_row + (in ? r : 0), in ? 4 : 0);
     }
   };
   // issue this thread's 16-byte copies of tile t into buffer b (gathered:
-  // rows from ai / gi, loaded by load_rows(t))
-  auto issue = [&](int64_t t, int b) {
+  // token rows from the assignments in `slot`, and each row's gate)
+  constexpr int NCH = TR / 16;                     // 16-byte chunks per thread per tile
+  auto issue = [&](int64_t t, int b, int slot) {
     const int rt = (int)(t / nct), ct = (int)(t - (int64_t)rt * nct);
 #pragma unroll
     for (int i = 0; i < NCH; ++i) {
@@ -240,29 +237,41 @@ __global__ void __launch_bounds__(256, 3) quant_dual_kernel(
           bytes = 16;
         }
       } else {
-        if (ai[i] >= 0) {
-          p = src + (size_t)(ai[i] / k) * ld + ct * 128 + 8 * c;
+        const int a = r < rows ? s_a[slot * TR + rl] : -1;
+        if (a >= n_assign && c == 0) report(status, MOE_ERR_BAD_INDEX);
+        const bool ok = a >= 0 && a < n_assign;
+        if (ok) {
+          p = src + (size_t)(a / k) * ld + ct * 128 + 8 * c;
           bytes = 16;
         }
-        if (SRC == 2 && c == 0) s_g[b * TR + rl] = gi[i];
+        if (SRC == 2 && c == 0) cp_async4(&s_g[b * TR + rl], ok ? gate + a : gate, ok ? 4 : 0);
       }
       cp_async16(&tbuf[b][rl][4 * c], p, bytes);
     }
   };
   int64_t t = blockIdx.x;
+  const int64_t G = gridDim.x;
+  if constexpr (SRC != 0) {
+    if (t < ntiles) copy_rows(t, 0);
+    if (t + G < ntiles) copy_rows(t + G, 1);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+  }
   if (t < ntiles) {
-    load_rows(t);
-    issue(t, 0);
-    if (t + gridDim.x < ntiles) load_rows(t + gridDim.x);
+    issue(t, 0, 0);
+    if (t + 2 * G < ntiles) copy_rows(t + 2 * G, 2);
   }
   cp_async_commit();
-  for (int b = 0; t < ntiles; t += gridDim.x, b ^= 1) {
+  if constexpr (SRC != 0) __syncthreads();   // slot 0 is read before it is refilled
+  for (int b = 0, j = 0; t < ntiles; t += G, b ^= 1, ++j) {
     const int rt = (int)(t / nct), ct = (int)(t - (int64_t)rt * nct);
     const int r0 = rt * TR, c0 = ct * 128;
     const int nrb = min(TR, rows - r0) / 32;        // 32-row blocks of this tile
-    if (t + gridDim.x < ntiles) {
-      issue(t + gridDim.x, b ^ 1);                 // next tile's copies in flight
-      if (t + 2 * (int64_t)gridDim.x < ntiles) load_rows(t + 2 * (int64_t)gridDim.x);
+    if (t + G < ntiles) {
+      issue(t + G, b ^ 1, (j + 1) % 3);            // next tile's copies in flight
+      // slot j % 3 (this tile's assignments) was read before the last barrier
+      if (t + 3 * G < ntiles) copy_rows(t + 3 * G, j % 3);
     }
     cp_async_commit();
     cp_async_wait_prev();
@@ -366,7 +375,7 @@ __global__ void __launch_bounds__(256, 3) quant_dual_kernel(
     }
     __syncthreads();   // buffer b and its gates are free for the next tiles
   }
-  asm volatile("cp.async.wait_all;" ::: "memory");
+  cp_async_wait_all();
 }
 
 int grid_cap() {
