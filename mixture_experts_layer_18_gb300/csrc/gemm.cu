@@ -144,9 +144,14 @@ struct Cfg {
   // stage's MMAs run (384 tensor cycles for block-scaled stages, 512 for
   // bf16), so on SM pairs a second producer warp loads B (and its scales)
   // while warp 0 loads A, and block-scaled runs add a warp that copies the
-  // scales into tensor memory.
+  // scales into tensor memory.  Measured on GB300 (one thread issuing from
+  // ready stages): four 192-column block-scaled MMAs take 384 tensor cycles
+  // but the issuing loop ~420 cycles with the scale copies inline, ~480
+  // with one barrier wait per stage and ~600 - 640 with two waits and a
+  // fence; the copier therefore signals once per SF_GROUP stages.
   static constexpr bool SPLIT_LOAD = PAIR == 2;
   static constexpr bool SPLIT_ISSUE = MX;          // scale-copier warp
+  static constexpr int SF_GROUP = 1;               // stages per scale-ready signal
   static constexpr int EXTRA_WARPS = (SPLIT_LOAD ? 1 : 0) + (SPLIT_ISSUE ? 1 : 0);
   static constexpr int THREADS = 64 + 32 * EPI_WARPS * EPI_GROUPS + 32 * EXTRA_WARPS;
   static constexpr int STG_BYTES = EPI_WARPS * EPI_GROUPS * 4096;   // staging (2 x 2 KB per warp)
@@ -169,6 +174,7 @@ struct Cfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
   static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
   static_assert(!MX || SF_COL0 + STAGES * 16 <= 512, "TMEM scale slots");
+  static_assert(!MX || STAGES % SF_GROUP == 0, "scale-ready groups tile the stage ring");
 };
 
 // ------------------------------------------------------------ tile decode
@@ -428,14 +434,25 @@ __device__ void producer_role(const EngineParams& P, const int* cum, int total, 
   }
 }
 
-// MMA issuer: one thread of the (leader) CTA.
+// MMA issuer: one thread of the (leader) CTA.  Each tcgen05.mma costs the
+// issuing thread a large share of the tensor time of a 192-column
+// block-scaled MMA, so the loop between MMAs is kept short: operand
+// descriptors are built once per tile and advanced by adding offsets, the
+// stage ring is walked incrementally, and a stage costs one barrier wait.
+// Data landed by TMA needs no tcgen05 fence; block-scaled stages wait only
+// for the scale copier's signal, which the copier gives after it saw the
+// stage's data land and after its scale copies into TMEM completed (one
+// signal per SF_GROUP stages), and fence after it (TMEM written by another
+// thread).
 template <class C>
 __device__ void mma_role(const EngineParams& P, const int* cum, int total, const int* s_po,
-                         const int* s_pt, uint8_t* stages, uint8_t* sfreg, uint64_t* full,
-                         uint64_t* empty,
+                         const int* s_pt, uint8_t* stages, uint64_t* full, uint64_t* empty,
                          uint64_t* tfull, uint64_t* tempty, uint64_t* drain, uint32_t tmem_base,
                          uint64_t* sfready, const WaitCtl& wc) {
   int it = 0, acc = 0;
+  int s = 0;            // it % STAGES
+  uint32_t ph = 0;      // (it / STAGES) & 1
+  uint32_t soff = 0;    // s * STAGE_BYTES in descriptor units (16 bytes)
   const uint32_t sbase = smem_u32(stages);
   const int cl = blockIdx.x / C::PAIR, ncl = gridDim.x / C::PAIR;
   for (int t = cl; t < total; t += ncl) {
@@ -458,48 +475,53 @@ __device__ void mma_role(const EngineParams& P, const int* cum, int total, const
     const uint32_t idesc = (C::MX ? (1u << 23) : (1u << 4)) | (C::FMT << 7) | (C::FMT << 10) |
                            (a_mn << 15) | (b_mn << 16) | ((uint32_t)(C::BN >> 3) << 17) |
                            ((uint32_t)((128 * C::PAIR) >> 4) << 24);
+    // stage-0 descriptors of this tile's operand layouts; a stage adds
+    // STAGE_BYTES / 16 and an MMA's K step 32 bytes (K-major) or one
+    // MN-major column block
+    const uint64_t a0 = a_mn ? smem_desc_sw128(sbase, C::ATOM_BYTES, 1024)
+                             : smem_desc_sw128(sbase, 16, 1024);
+    const uint64_t b0 = b_mn ? smem_desc_sw128(sbase + C::A_BYTES, C::ATOM_BYTES, 1024)
+                             : smem_desc_sw128(sbase + C::A_BYTES, 16, 1024);
+    const uint32_t ak = a_mn ? C::MN_KSTEP_BYTES >> 4 : 2, bk = b_mn ? C::MN_KSTEP_BYTES >> 4 : 2;
     bool ok = true;
-    for (int kb = 0; kb < ti.nk; ++kb, ++it) {
-      const int s = it % C::STAGES;
-      if (!wait_bar_p<C>(&full[s], (it / C::STAGES) & 1, wc)) { ok = false; break; }
-      // block-scaled: the scale copier has put this stage's scales in TMEM
-      if (C::SPLIT_ISSUE && !wait_bar_p<C>(&sfready[s], (it / C::STAGES) & 1, wc)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t aA = sbase + s * C::STAGE_BYTES;
-      const uint32_t aB = aA + C::A_BYTES;
-      uint32_t sf_slot = 0;
-      if constexpr (C::MX) sf_slot = tmem_base + C::SF_COL0 + s * 16;
-      if constexpr (C::MX && !C::SPLIT_ISSUE) {
-        // scales of this stage into its TMEM slot: A at +0..3, B at +4..
-        const uint32_t aS = smem_u32(sfreg) + s * C::SF_BYTES;
-#pragma unroll
-        for (int j = 0; j < 1 + C::SFB_BYTES / 512; ++j) {
-          if constexpr (C::PAIR == 2)
-            tmem_cp_32x128b_x4_pair(sf_slot + 4 * j, smem_desc_rows16(aS + 512 * j));
-          else
-            tmem_cp_32x128b_x4(sf_slot + 4 * j, smem_desc_rows16(aS + 512 * j));
+    for (int kb = 0; kb < ti.nk; ++kb) {
+      if constexpr (C::MX) {
+        if (it % C::SF_GROUP == 0) {
+          const int q = it / C::SF_GROUP;
+          if (!wait_bar_p<C>(&sfready[q % (C::STAGES / C::SF_GROUP)], ph, wc)) { ok = false; break; }
+          tc_fence_after();
         }
+      } else {
+        if (!wait_bar_p<C>(&full[s], ph, wc)) { ok = false; break; }
       }
+      const uint32_t sf_slot = tmem_base + C::SF_COL0 + s * 16;
 #pragma unroll
       for (int kk = 0; kk < C::KSTEPS; ++kk) {
-        const uint64_t ad = a_mn ? smem_desc_sw128(aA + kk * C::MN_KSTEP_BYTES, C::ATOM_BYTES, 1024)
-                                 : smem_desc_sw128(aA + kk * 32, 16, 1024);
-        const uint64_t bd = b_mn ? smem_desc_sw128(aB + kk * C::MN_KSTEP_BYTES, C::ATOM_BYTES, 1024)
-                                 : smem_desc_sw128(aB + kk * 32, 16, 1024);
+        const uint64_t ad = a0 + soff + kk * ak;
+        const uint64_t bd = b0 + soff + kk * bk;
+        const uint32_t accum = (kb | kk) != 0;
         if constexpr (C::MX && C::PAIR == 2)
           mma_mxf8_pair(d, ad, bd, idesc | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), sf_slot,
-                        sf_slot + 4, (kb | kk) != 0);
+                        sf_slot + 4, accum);
         else if constexpr (C::MX)
           mma_mxf8(d, ad, bd, idesc | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), sf_slot,
-                   sf_slot + 4, (kb | kk) != 0);
+                   sf_slot + 4, accum);
         else if constexpr (C::PAIR == 2)
-          mma_f16_pair(d, ad, bd, idesc, (kb | kk) != 0);
+          mma_f16_pair(d, ad, bd, idesc, accum);
         else if constexpr (C::ES == 2)
-          mma_f16(d, ad, bd, idesc, (kb | kk) != 0);
+          mma_f16(d, ad, bd, idesc, accum);
         else
-          mma_tf32(d, ad, bd, idesc, (kb | kk) != 0);
+          mma_tf32(d, ad, bd, idesc, accum);
       }
       if constexpr (C::PAIR == 2) tc_commit_pair(&empty[s], 3); else tc_commit(&empty[s]);
+      ++it;
+      if (++s == C::STAGES) {
+        s = 0;
+        ph ^= 1;
+        soff = 0;
+      } else {
+        soff += C::STAGE_BYTES >> 4;
+      }
     }
     if (!ok) break;
     if constexpr (C::PAIR == 2) tc_commit_pair(&tfull[buf], 3); else tc_commit(&tfull[buf]);
@@ -512,18 +534,19 @@ __device__ void mma_role(const EngineParams& P, const int* cum, int total, const
 
 // Scale copier (block-scaled runs, one thread of the leader CTA): once a
 // stage's operands and scale atoms have landed, copies the scales into that
-// stage's TMEM slot (A at +0..3, B at +4..11) and signals sfready[stage]
-// when the copies have completed.  A slot is rewritten only after the stage
-// was refilled, i.e. after the MMAs that read its previous scales finished.
+// stage's TMEM slot (A at +0..3, B at +4..11), and after every SF_GROUP
+// stages (and after its last one) signals sfready[group] once those copies
+// have completed.  A slot is rewritten only after the stage was refilled,
+// i.e. after the MMAs that read its previous scales finished.
 template <class C>
 __device__ void sf_role(const EngineParams& P, const int* cum, int total, const int* s_po,
                         const int* s_pt, uint8_t* sfreg, uint64_t* full, uint64_t* sfready,
                         uint64_t* drain, uint32_t tmem_base, const WaitCtl& wc) {
   int it = 0;
   const int cl = blockIdx.x / C::PAIR, ncl = gridDim.x / C::PAIR;
-  for (int t = cl; t < total; t += ncl) {
+  bool ok = true;
+  for (int t = cl; ok && t < total; t += ncl) {
     const Tile ti = decode_tile<C>(P, cum, s_po, s_pt, t, 0);
-    bool ok = true;
     for (int kb = 0; kb < ti.nk; ++kb, ++it) {
       const int s = it % C::STAGES;
       if (!wait_bar_p<C>(&full[s], (it / C::STAGES) & 1, wc)) { ok = false; break; }
@@ -537,9 +560,16 @@ __device__ void sf_role(const EngineParams& P, const int* cum, int total, const 
         else
           tmem_cp_32x128b_x4(slot + 4 * j, smem_desc_rows16(aS + 512 * j));
       }
-      if constexpr (C::PAIR == 2) tc_commit_pair(&sfready[s], 1); else tc_commit(&sfready[s]);
+      if (it % C::SF_GROUP == C::SF_GROUP - 1) {
+        uint64_t* bar = &sfready[(it / C::SF_GROUP) % (C::STAGES / C::SF_GROUP)];
+        if constexpr (C::PAIR == 2) tc_commit_pair(bar, 1); else tc_commit(bar);
+      }
     }
-    if (!ok) break;
+  }
+  // a last, partial group is signalled too (the MMA issuer waits for it)
+  if (ok && it % C::SF_GROUP != 0) {
+    uint64_t* bar = &sfready[(it / C::SF_GROUP) % (C::STAGES / C::SF_GROUP)];
+    if constexpr (C::PAIR == 2) tc_commit_pair(bar, 1); else tc_commit(bar);
   }
   // every copy completed before TMEM is released
   if constexpr (C::PAIR == 2) tc_commit_pair(drain, 1); else tc_commit(drain);
@@ -1092,7 +1122,7 @@ __global__ void __launch_bounds__(Cfg<In, BN, PAIR>::THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     if ((threadIdx.x & 31) == 0 && rank == 0)
-      mma_role<C>(P, cum, total, s_po, s_pt, stages, sfreg, full, empty, tfull, tempty, drain,
+      mma_role<C>(P, cum, total, s_po, s_pt, stages, full, empty, tfull, tempty, drain,
                   tmem_base, sfready, wc);
     __syncwarp();
   } else if (warp < EPI_END) {
