@@ -278,8 +278,9 @@ def run_reference(args):
 def _per_config(cfg, mode, d, steps, warmup, peaks):
     """fwd / bwd / step ms of one workload and mode on already-resident inputs
     ``d`` (device tensors), with the grouped-GEMM launch times from the
-    library's event hook (in the MXFP8 modes that bracket also holds the
-    quantise passes between the GEMM launches)."""
+    library's event hooks: the bracket from the first to the last GEMM launch
+    of a call (in the MXFP8 modes it also holds the quantise passes between
+    the launches) and the sum of the GEMM launches alone."""
     import torch
 
     import mixture_experts_layer_18_gb300 as M
@@ -306,16 +307,22 @@ def _per_config(cfg, mode, d, steps, warmup, peaks):
 
     pf = [(ev(), ev()) for _ in range(steps)]
     pb = [(ev(), ev()) for _ in range(steps)]
-    for a, b in pf + pb:       # materialise the event handles (torch creates them lazily)
-        a.record()
+    lf = [[(ev(), ev()) for _ in range(2)] for _ in range(steps)]   # per GEMM launch
+    lb = [[(ev(), ev()) for _ in range(2)] for _ in range(steps)]
+    for a, b in pf + pb + [x for row in lf + lb for x in row]:
+        a.record()             # materialise the event handles (torch creates them lazily)
         b.record()
     t0, t1 = ev(), ev()
     torch.cuda.synchronize()
     t0.record()
     for i in range(steps):
         M.moe_set_gemm_events(M.MOE_WS_FORWARD, pf[i][0].cuda_event, pf[i][1].cuda_event)
+        M.moe_set_gemm_launch_events(M.MOE_WS_FORWARD, [a.cuda_event for a, _ in lf[i]],
+                                     [b.cuda_event for _, b in lf[i]])
         fwd()
         M.moe_set_gemm_events(M.MOE_WS_BACKWARD, pb[i][0].cuda_event, pb[i][1].cuda_event)
+        M.moe_set_gemm_launch_events(M.MOE_WS_BACKWARD, [a.cuda_event for a, _ in lb[i]],
+                                     [b.cuda_event for _, b in lb[i]])
         bwd()
     t1.record()
     torch.cuda.synchronize()
@@ -336,6 +343,8 @@ def _per_config(cfg, mode, d, steps, warmup, peaks):
     fwd_ms, bwd_ms = timed(fwd), timed(bwd)
     gf = statistics.mean(a.elapsed_time(b) for a, b in pf)
     gb = statistics.mean(a.elapsed_time(b) for a, b in pb)
+    gf1 = statistics.mean(sum(a.elapsed_time(b) for a, b in row) for row in lf)
+    gb1 = statistics.mean(sum(a.elapsed_time(b) for a, b in row) for row in lb)
     out = {"workload": _workload_desc(cfg), "mode": mode, "steps": steps, "warmup": warmup,
            "ms_per_step": step, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
            "tflops": (cfg.fwd_flops() + cfg.bwd_flops()) / (step * 1e-3) / 1e12,
@@ -349,10 +358,14 @@ def _per_config(cfg, mode, d, steps, warmup, peaks):
             "fwd_launch_ms": gf, "bwd_launch_ms": gb,
             "fwd_frac": cfg.fwd_flops() / (gf * 1e-3) / 1e12 / pk_f,
             "bwd_frac": cfg.bwd_flops() / (gb * 1e-3) / 1e12 / pk_b,
+            "fwd_gemm_only_ms": gf1, "bwd_gemm_only_ms": gb1,
+            "fwd_gemm_only_frac": cfg.fwd_flops() / (gf1 * 1e-3) / 1e12 / pk_f,
+            "bwd_gemm_only_frac": cfg.bwd_flops() / (gb1 * 1e-3) / 1e12 / pk_b,
             "peak_tflops_fwd": pk_f, "peak_tflops_bwd": pk_b,
             "note": ("bf16 sustained measured peak" + (" x 2 (nominal fp8/bf16 ratio) where MXFP8"
                      if mode != "bf16" else "")
-                     + ("; the bracket includes the quantise passes between the GEMM launches"
+                     + ("; the bracket includes the quantise passes between the GEMM launches, "
+                        "gemm_only sums the two GEMM launches of each call"
                         if mode != "bf16" else ""))}
     del L, io
     torch.cuda.empty_cache()
@@ -417,7 +430,9 @@ def run_gpu(args):
     K = args.steps
     pairs_b = [(ev(), ev()) for _ in range(K)]
     pairs_f = [(ev(), ev()) for _ in range(K)]
-    for a, b in pairs_b + pairs_f:       # materialise the event handles
+    lb = [[(ev(), ev()) for _ in range(2)] for _ in range(K)]   # per GEMM launch
+    lf = [[(ev(), ev()) for _ in range(2)] for _ in range(K)]
+    for a, b in pairs_b + pairs_f + [x for row in lb + lf for x in row]:   # materialise handles
         a.record()
         b.record()
     torch.cuda.synchronize()
@@ -431,8 +446,12 @@ def run_gpu(args):
     t0.record()
     for i in range(K):
         M.moe_set_gemm_events(M.MOE_WS_FORWARD, pairs_f[i][0].cuda_event, pairs_f[i][1].cuda_event)
+        M.moe_set_gemm_launch_events(M.MOE_WS_FORWARD, [a.cuda_event for a, _ in lf[i]],
+                                     [b.cuda_event for _, b in lf[i]])
         fwd()
         M.moe_set_gemm_events(M.MOE_WS_BACKWARD, pairs_b[i][0].cuda_event, pairs_b[i][1].cuda_event)
+        M.moe_set_gemm_launch_events(M.MOE_WS_BACKWARD, [a.cuda_event for a, _ in lb[i]],
+                                     [b.cuda_event for _, b in lb[i]])
         bwd()
     t1.record()
     torch.cuda.synchronize()
@@ -440,8 +459,12 @@ def run_gpu(args):
     barrier()
     clk = clocks.stop()
     ms_step = t0.elapsed_time(t1) / K
-    gemm_b = statistics.mean(a.elapsed_time(b) for a, b in pairs_b)
-    gemm_f = statistics.mean(a.elapsed_time(b) for a, b in pairs_f)
+    # the GEMM launches alone (summed per call), and the bracket from the
+    # first to the last of them (MXFP8: with the quantise passes in between)
+    gemm_b = statistics.mean(sum(a.elapsed_time(b) for a, b in row) for row in lb)
+    gemm_f = statistics.mean(sum(a.elapsed_time(b) for a, b in row) for row in lf)
+    bracket_b = statistics.mean(a.elapsed_time(b) for a, b in pairs_b)
+    bracket_f = statistics.mean(a.elapsed_time(b) for a, b in pairs_f)
     if L.device_status() != 0:
         raise RuntimeError(f"device status {L.device_status()} after timed steps")
 
@@ -543,8 +566,9 @@ def run_gpu(args):
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
 
     # ---- max over ranks
-    ms_step, e2e_ms, fwd_ms, bwd_ms, gemm_b, gemm_f, full_ms = max_over_ranks(
-        [ms_step, e2e_ms, fwd_ms, bwd_ms, gemm_b, gemm_f, full_ms], world, "cuda")
+    ms_step, e2e_ms, fwd_ms, bwd_ms, gemm_b, gemm_f, full_ms, bracket_b, bracket_f = max_over_ranks(
+        [ms_step, e2e_ms, fwd_ms, bwd_ms, gemm_b, gemm_f, full_ms, bracket_b, bracket_f], world,
+        "cuda")
 
     flops_step = cfg.fwd_flops() + cfg.bwd_flops()
     value = job_throughput(flops_step, world, ms_step)
@@ -570,7 +594,8 @@ def run_gpu(args):
          "mixture_experts_layer_18_gb300/csrc/common.cuh"])
     kname = ("moe_gemm_kernel<bf16,256,2>: the backward's two co-scheduled GEMM launches "
              "({D, dW2}, {dX, dW13})" if not mx_b
-             else "MXFP8 backward: its quantise passes and 2 co-scheduled GEMM launches")
+             else "moe_gemm_kernel<e4m3,192,2>: the MXFP8 backward's two co-scheduled GEMM "
+             "launches ({D, dW2}, {dX, dW13})")
     out = {
         "metric": "moe_layer_step_tflops", "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -591,9 +616,12 @@ def run_gpu(args):
                      "bound": "tensor", "achieved": ach_b, "peak": peak_b, "unit": "TFLOP/s",
                      "frac": ach_b / peak_b, "traffic": traffic,
                      "peak_source": peak_note, "launch_ms": gemm_b,
+                     "launch_ms_how": "sum of the two launches' CUDA-event times per step",
+                     "bracket_ms": bracket_b,
                      "frac_of_burst_peak": ach_b / (peak_burst * peak_b / peak)},
         "roofline_forward_gemms": {"achieved": ach_f, "peak": peak_f, "frac": ach_f / peak_f,
                                    "unit": "TFLOP/s", "launch_ms": gemm_f,
+                                   "bracket_ms": bracket_f,
                                    "frac_of_burst_peak": ach_f / (peak_burst * peak_f / peak)},
         "e2e": {"value": world * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,

@@ -314,11 +314,20 @@ moe_status moe_debug_occupy(int ctas, int smem_bytes, int64_t duration_ns, void*
 /* Timing hook for kernel-level measurement.  `start` and `stop` are
  * cudaEvent_t handles (as void*) created by the caller.  The next call of the
  * kind `which` (MOE_WS_FORWARD: the two grouped-GEMM launches of moe_forward;
- * MOE_WS_BACKWARD: the co-scheduled gradient-GEMM launch of moe_backward)
- * records `start` on its stream just before those launches and `stop` just
- * after them, then forgets the events.  NULL events cancel a pending hook.
- * Process-wide; not thread-safe against concurrent calls. */
+ * MOE_WS_BACKWARD: the gradient-GEMM launches of moe_backward) records
+ * `start` on its stream just before the first of those launches and `stop`
+ * just after the last, then forgets the events; in the MXFP8 modes the
+ * quantisation passes between the launches fall inside.  NULL events cancel
+ * a pending hook.  Process-wide; not thread-safe against concurrent calls. */
 void moe_set_gemm_events(int which, void* start, void* stop);
+
+/* Per-launch form of the same hook: the next call of the kind `which`
+ * records start[i] just before and stop[i] just after its i-th grouped-GEMM
+ * launch, for i < n (n at most 8; launches past n are not timed), then
+ * forgets the events.  Each array holds n cudaEvent_t handles (as void*)
+ * created by the caller; a NULL array, n <= 0 or a NULL handle cancels a
+ * pending hook.  Process-wide; not thread-safe against concurrent calls. */
+void moe_set_gemm_launch_events(int which, void* const* start, void* const* stop, int n);
 
 #ifdef __cplusplus
 }

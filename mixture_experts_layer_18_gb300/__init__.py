@@ -20,7 +20,7 @@ __all__ = [
     "MOE_DEBUG_NEVER_READY", "MOE_DEBUG_SINGLE_CTA", "MOE_DEBUG_SPLIT_BACKWARD", "MOE_DEBUG_ONE_LAUNCH_BACKWARD", "moe_dims", "moe_route_out", "moe_saved_layout",
     "lib", "header_functions", "moe_max_rows", "moe_workspace_size",
     "moe_saved_layout_of", "moe_route", "moe_route_noalloc", "moe_route_backward", "moe_forward", "moe_backward",
-    "moe_quantize_mxfp8", "moe_quantize_mxfp8_dual", "moe_status_string", "moe_set_debug", "moe_set_gemm_events", "moe_debug_occupy",
+    "moe_quantize_mxfp8", "moe_quantize_mxfp8_dual", "moe_status_string", "moe_set_debug", "moe_set_gemm_events", "moe_set_gemm_launch_events", "moe_debug_occupy",
     "MoEError",
 ]
 
@@ -81,6 +81,7 @@ _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [_c_int]),
     "moe_set_debug": (None, [_c_int, _i64]),
     "moe_set_gemm_events": (None, [_c_int, _vp, _vp]),
+    "moe_set_gemm_launch_events": (None, [_c_int, _vp, _vp, _c_int]),
     "moe_debug_occupy": (_c_int, [_c_int, _c_int, _i64, _vp]),
 }
 
@@ -178,3 +179,13 @@ def moe_debug_occupy(ctas: int, smem_bytes: int, duration_ns: int, stream) -> in
 def moe_set_gemm_events(which: int, start, stop) -> None:
     """start / stop: cudaEvent_t handles (ints) or None."""
     lib().moe_set_gemm_events(which, start, stop)
+
+
+def moe_set_gemm_launch_events(which: int, starts, stops) -> None:
+    """starts / stops: equal-length lists of cudaEvent_t handles (ints); the
+    next call of kind `which` records them around its grouped-GEMM launches
+    in order.  An empty list cancels a pending hook."""
+    n = min(len(starts), len(stops))
+    a = (ctypes.c_void_p * max(n, 1))(*starts[:n])
+    b = (ctypes.c_void_p * max(n, 1))(*stops[:n])
+    lib().moe_set_gemm_launch_events(which, a if n else None, b if n else None, n)

@@ -11,13 +11,25 @@
 namespace moe {
 
 namespace {
+constexpr int kMaxLaunchEvents = 8;
 std::atomic<int> g_debug_flags{0};
 std::atomic<long long> g_wait_ns{1000000000LL};   // one second
 // one-shot timing events per call kind (forward, backward)
 std::atomic<void*> g_ev_start[3] = {nullptr, nullptr, nullptr};
 std::atomic<void*> g_ev_stop[3] = {nullptr, nullptr, nullptr};
 
-struct EventScope {   // records the pending hook's events around a launch group
+// one-shot events around each grouped-GEMM launch of the next call of a kind
+struct LaunchEvents {
+  void* start[kMaxLaunchEvents];
+  void* stop[kMaxLaunchEvents];
+  int n;
+};
+LaunchEvents g_launch_ev[3];
+std::atomic<int> g_launch_armed[3] = {0, 0, 0};
+thread_local const LaunchEvents* t_launch_ev = nullptr;   // the running call's hook
+thread_local int t_launch_i = 0;
+
+struct EventScope {   // records the pending hooks' events around a launch group
   cudaEvent_t stop = nullptr;
   cudaStream_t s;
   EventScope(int which, cudaStream_t st) : s(st) {
@@ -27,13 +39,32 @@ struct EventScope {   // records the pending hook's events around a launch group
       cudaEventRecord(static_cast<cudaEvent_t>(a), s);
       stop = static_cast<cudaEvent_t>(b);
     }
+    if (g_launch_armed[which].exchange(0)) {
+      t_launch_ev = &g_launch_ev[which];
+      t_launch_i = 0;
+    }
   }
   void finish() {
     if (stop) cudaEventRecord(stop, s);
     stop = nullptr;
+    t_launch_ev = nullptr;
   }
   ~EventScope() { finish(); }
 };
+
+// A grouped-GEMM launch, with the running call's per-launch events if any.
+cudaError_t engine(const EngineLaunch& L, cudaStream_t s, moe_status* st) {
+  const LaunchEvents* h = t_launch_ev;
+  const int i = t_launch_i;
+  const bool rec = h && i < h->n;
+  if (rec) cudaEventRecord(static_cast<cudaEvent_t>(h->start[i]), s);
+  const cudaError_t e = launch_engine(L, s, st);
+  if (rec) {
+    cudaEventRecord(static_cast<cudaEvent_t>(h->stop[i]), s);
+    t_launch_i = i + 1;
+  }
+  return e;
+}
 }  // namespace
 
 uint64_t wait_limit_ns() { return (uint64_t)g_wait_ns.load(); }
@@ -381,7 +412,7 @@ moe_status forward_mx(const moe_dims* d, const void* X, const void* W13, const v
       g.enc_col_kg = rp / 128;
     }
     g.out2 = d->save_for_backward ? h13 : nullptr; g.ld_out2 = 2 * I;
-    MOE_TRY(launch_engine(L, s, &st));
+    MOE_TRY(engine(L, s, &st));
     if (st != MOE_OK) return st;
   }
   // W2: row-wise for D (saved), transposed column-wise for the down GEMM
@@ -397,7 +428,7 @@ moe_status forward_mx(const moe_dims* d, const void* X, const void* W13, const v
     g.N = H; g.K = I;
     g.out = zg; g.ld_out = H;
     g.gate = r->gate; g.assign_of_row = r->assign_of_row; g.n_assign = d->T * d->top_k;
-    MOE_TRY(launch_engine(L, s, &st));
+    MOE_TRY(engine(L, s, &st));
     if (st != MOE_OK) return st;
   }
   return MOE_OK;
@@ -469,7 +500,7 @@ moe_status backward_mx(const moe_dims* d, const void* dY, const void* W13, const
     gw2.b = dygc.q; gw2.b_rows = H; gw2.b_cols = rp; gw2.sfb = dygc.sf; gw2.sfb_bytes = dygc.sf_bytes; gw2.sfb_kg = kgt;
     gw2.M = I; gw2.N = H;
     gw2.out = dW2; gw2.ld_out = H;
-    MOE_TRY(launch_engine(L, s, &st));
+    MOE_TRY(engine(L, s, &st));
     if (st != MOE_OK) return st;
   }
   if (!saved_mx) {
@@ -495,7 +526,7 @@ moe_status backward_mx(const moe_dims* d, const void* dY, const void* W13, const
     gw.b = dh13c.q; gw.b_rows = 2 * I; gw.b_cols = rp; gw.sfb = dh13c.sf; gw.sfb_bytes = dh13c.sf_bytes; gw.sfb_kg = kgt;
     gw.M = H; gw.N = 2 * I;
     gw.out = dW13; gw.ld_out = 2 * I;
-    MOE_TRY(launch_engine(L, s, &st));
+    MOE_TRY(engine(L, s, &st));
     if (st != MOE_OK) return st;
   }
   return MOE_OK;
@@ -542,6 +573,20 @@ void moe_set_gemm_events(int which, void* start, void* stop) {
   if (which != MOE_WS_FORWARD && which != MOE_WS_BACKWARD) return;
   g_ev_start[which].store(start && stop ? start : nullptr);
   g_ev_stop[which].store(start && stop ? stop : nullptr);
+}
+
+void moe_set_gemm_launch_events(int which, void* const* start, void* const* stop, int n) {
+  if (which != MOE_WS_FORWARD && which != MOE_WS_BACKWARD) return;
+  g_launch_armed[which].store(0);
+  if (!start || !stop || n <= 0) return;
+  LaunchEvents& h = g_launch_ev[which];
+  h.n = n < kMaxLaunchEvents ? n : kMaxLaunchEvents;
+  for (int i = 0; i < h.n; ++i) {
+    if (!start[i] || !stop[i]) return;   // incomplete list: stays cancelled
+    h.start[i] = start[i];
+    h.stop[i] = stop[i];
+  }
+  g_launch_armed[which].store(1);
 }
 
 void moe_set_debug(int flags, int64_t wait_limit_ns) {
@@ -668,7 +713,7 @@ moe_status moe_forward(const moe_dims* d, const void* X, const void* W13, const 
     g.N = 2 * d->I; g.K = d->H; g.I = d->I;
     g.out = act; g.ld_out = d->I;
     g.out2 = d->save_for_backward ? h13 : nullptr; g.ld_out2 = 2 * d->I;
-    MOE_TRY(launch_engine(L, s, &st));
+    MOE_TRY(engine(L, s, &st));
     if (st != MOE_OK) return st;
   }
   {
@@ -690,7 +735,7 @@ moe_status moe_forward(const moe_dims* d, const void* X, const void* W13, const 
     if (!gate_on_act(d)) {  // Z = gate * (A W2)
       g.gate = r->gate; g.assign_of_row = r->assign_of_row; g.n_assign = n_assign;
     }
-    MOE_TRY(launch_engine(L, s, &st));
+    MOE_TRY(engine(L, s, &st));
     if (st != MOE_OK) return st;
   }
   timing.finish();
@@ -817,7 +862,7 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
       L.nprob = 1;
       for (const GemmDesc& gp : parts) {
         L.prob[0] = gp;
-        MOE_TRY(launch_engine(L, s, &st));
+        MOE_TRY(engine(L, s, &st));
         if (st != MOE_OK) return st;
       }
     } else if (one_launch) {
@@ -832,7 +877,7 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
       L.prob[1] = gw2;
       L.prob[2] = gx;
       L.prob[3] = gw13;
-      MOE_TRY(launch_engine(L, s, &st));
+      MOE_TRY(engine(L, s, &st));
       if (st != MOE_OK) return st;
     } else {
       // Co-scheduled in two persistent launches ([OB] "Overlapping Backward
@@ -843,11 +888,11 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
       L.nprob = 2;
       L.prob[0] = gd;
       L.prob[1] = gw2;
-      MOE_TRY(launch_engine(L, s, &st));
+      MOE_TRY(engine(L, s, &st));
       if (st != MOE_OK) return st;
       L.prob[0] = gx;
       L.prob[1] = gw13;
-      MOE_TRY(launch_engine(L, s, &st));
+      MOE_TRY(engine(L, s, &st));
       if (st != MOE_OK) return st;
     }
   } else {
@@ -862,7 +907,7 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
     L.nprob = 2;
     L.prob[0] = gd;
     L.prob[1] = gw2;
-    MOE_TRY(launch_engine(L, s, &st));
+    MOE_TRY(engine(L, s, &st));
     if (st != MOE_OK) return st;
     MOE_TRY(launch_transpose_f32(static_cast<const float*>(dh13), dh13_t, 1, rows, 2 * d->I, lt, s));
     gw13.a = xp_t; gw13.a_rows = d->H; gw13.a_cols = lt;
@@ -870,7 +915,7 @@ moe_status moe_backward(const moe_dims* d, const void* dY, const void* W13, cons
     L.nprob = 2;
     L.prob[0] = gx;
     L.prob[1] = gw13;
-    MOE_TRY(launch_engine(L, s, &st));
+    MOE_TRY(engine(L, s, &st));
     if (st != MOE_OK) return st;
   }
   timing.finish();
