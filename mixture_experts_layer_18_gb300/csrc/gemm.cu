@@ -154,6 +154,15 @@ struct Cfg {
   static constexpr int SF_GROUP = 1;               // stages per scale-ready signal
   static constexpr int EXTRA_WARPS = (SPLIT_LOAD ? 1 : 0) + (SPLIT_ISSUE ? 1 : 0);
   static constexpr int THREADS = 64 + 32 * EPI_WARPS * EPI_GROUPS + 32 * EXTRA_WARPS;
+  // Block-scaled CTAs put the four single-thread roles (A loader, MMA, B
+  // loader, scale copier) in warpgroup 0 and the two epilogue groups in
+  // warpgroups 1 and 2, so the roles can hand registers to the epilogues
+  // (setmaxnreg: 4 x 32 x ROLE_REGS + 8 x 32 x EPI_REGS <= 384 x 168, the
+  // registers the CTA is launched with); other CTAs keep the epilogue at
+  // warps 2.. and the B loader after it.
+  static constexpr bool REG_SPLIT = MX && PAIR == 2;
+  static constexpr int EPI_FIRST = REG_SPLIT ? 4 : 2;     // first epilogue warp
+  static constexpr int ROLE_REGS = 64, EPI_REGS = 216;
   static constexpr int STG_BYTES = EPI_WARPS * EPI_GROUPS * 4096;   // staging (2 x 2 KB per warp)
   static constexpr int FIXED_BYTES = STG_BYTES + 1024 /*align*/ + 512 /*bars*/ +
                                      2 * (kMaxE + 1) * 4 + kMaxE * 4 /*counts*/ + 64 + 256;
@@ -753,12 +762,12 @@ __device__ void epilogue_role(const EngineParams& P, const int* cum, int total, 
   constexpr int ET = C::EPI_WARPS * 32;      // threads of an epilogue group
   constexpr int NG = C::EPI_GROUPS;
   static_assert(NG == 1 || NG == C::NACC, "one accumulator per epilogue group");
-  const int ew = (threadIdx.x >> 5) - 2;     // epilogue warp
+  const int ew = (threadIdx.x >> 5) - C::EPI_FIRST;   // epilogue warp
   const int grp = ew / C::EPI_WARPS;         // its group: tiles acc with acc % NG == grp
   const int q = (threadIdx.x >> 5) & 3;      // TMEM lane quarter of this warp
   const int lane = threadIdx.x & 31;
   const int r = q * 32 + lane;               // tile row of this thread
-  const bool leader = threadIdx.x == 64 + grp * ET;   // first thread of the group
+  const bool leader = threadIdx.x == 32 * C::EPI_FIRST + grp * ET;   // first thread of the group
   const int cl = blockIdx.x / C::PAIR, ncl = gridDim.x / C::PAIR;
   uint8_t* sb0 = stg + ew * 4096;
   uint8_t* sb1 = sb0 + 2048;
@@ -1114,27 +1123,50 @@ __global__ void __launch_bounds__(Cfg<In, BN, PAIR>::THREADS, 1)
   const int total = cum[P.nprob];
   const WaitCtl wc{abort_flag, P.status, P.wait_ns};
 
-  constexpr int EPI_END = 2 + C::EPI_WARPS * C::EPI_GROUPS;   // first warp after the epilogue
-  if (warp == 0) {
-    if ((threadIdx.x & 31) == 0)
-      producer_role<C>(P, cum, total, s_po, s_pt, rank, stages, sfreg, full, empty, wc,
-                       C::SPLIT_LOAD ? 0 : -1);
-    __syncwarp();
-  } else if (warp == 1) {
-    if ((threadIdx.x & 31) == 0 && rank == 0)
-      mma_role<C>(P, cum, total, s_po, s_pt, stages, full, empty, tfull, tempty, drain,
-                  tmem_base, sfready, wc);
-    __syncwarp();
-  } else if (warp < EPI_END) {
-    epilogue_role<C, Out>(P, cum, total, s_po, s_pt, rank, tfull, tempty, tmem_base, s_go, stg, wc);
-  } else if (C::SPLIT_LOAD && warp == EPI_END) {
-    if ((threadIdx.x & 31) == 0)
-      producer_role<C>(P, cum, total, s_po, s_pt, rank, stages, sfreg, full, empty, wc, 1);
-    __syncwarp();
-  } else if constexpr (C::SPLIT_ISSUE) {
-    if ((threadIdx.x & 31) == 0 && rank == 0)
-      sf_role<C>(P, cum, total, s_po, s_pt, sfreg, full, sfready, drain2, tmem_base, wc);
-    __syncwarp();
+  if constexpr (C::REG_SPLIT) {
+    static_assert(C::THREADS == 384 && C::EPI_WARPS * C::EPI_GROUPS == 8, "three warpgroups");
+    static_assert(128 * C::ROLE_REGS + 256 * C::EPI_REGS <= 384 * 168, "register split");
+    if (warp < 4) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::ROLE_REGS));
+      if ((threadIdx.x & 31) == 0) {
+        if (warp == 0)
+          producer_role<C>(P, cum, total, s_po, s_pt, rank, stages, sfreg, full, empty, wc, 0);
+        else if (warp == 1 && rank == 0)
+          mma_role<C>(P, cum, total, s_po, s_pt, stages, full, empty, tfull, tempty, drain,
+                      tmem_base, sfready, wc);
+        else if (warp == 2)
+          producer_role<C>(P, cum, total, s_po, s_pt, rank, stages, sfreg, full, empty, wc, 1);
+        else if (warp == 3 && rank == 0)
+          sf_role<C>(P, cum, total, s_po, s_pt, sfreg, full, sfready, drain2, tmem_base, wc);
+      }
+      __syncwarp();
+    } else {
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::EPI_REGS));
+      epilogue_role<C, Out>(P, cum, total, s_po, s_pt, rank, tfull, tempty, tmem_base, s_go, stg, wc);
+    }
+  } else {
+    constexpr int EPI_END = 2 + C::EPI_WARPS * C::EPI_GROUPS;   // first warp after the epilogue
+    if (warp == 0) {
+      if ((threadIdx.x & 31) == 0)
+        producer_role<C>(P, cum, total, s_po, s_pt, rank, stages, sfreg, full, empty, wc,
+                         C::SPLIT_LOAD ? 0 : -1);
+      __syncwarp();
+    } else if (warp == 1) {
+      if ((threadIdx.x & 31) == 0 && rank == 0)
+        mma_role<C>(P, cum, total, s_po, s_pt, stages, full, empty, tfull, tempty, drain,
+                    tmem_base, sfready, wc);
+      __syncwarp();
+    } else if (warp < EPI_END) {
+      epilogue_role<C, Out>(P, cum, total, s_po, s_pt, rank, tfull, tempty, tmem_base, s_go, stg, wc);
+    } else if (C::SPLIT_LOAD && warp == EPI_END) {
+      if ((threadIdx.x & 31) == 0)
+        producer_role<C>(P, cum, total, s_po, s_pt, rank, stages, sfreg, full, empty, wc, 1);
+      __syncwarp();
+    } else if constexpr (C::SPLIT_ISSUE) {
+      if ((threadIdx.x & 31) == 0 && rank == 0)
+        sf_role<C>(P, cum, total, s_po, s_pt, sfreg, full, sfready, drain2, tmem_base, wc);
+      __syncwarp();
+    }
   }
   tc_fence_before();
   __syncthreads();
